@@ -1,0 +1,399 @@
+#!/usr/bin/env python
+"""(O, P) SDPA forward benchmark on one GB300 (or N independent replicas).
+
+One step = one materialised-probability SDPA forward over the workload: scores,
+masking, row statistics, exact P = exp(S - lse), P V and the stores of O and P,
+all in the library's CUDA kernels, called through the C ABI.
+
+Default workload: prefill 1k D64 (fp16, B=2, H=8, Sq=Skv=1024, D=64, causal),
+the shape of the perf-gate baseline of FlagOS-OP PR #10 "feat: add sdpa_math
+operator".  ``--config`` selects another of the synthetic workloads.
+
+Timing: W warm-up steps, then exactly K timed steps, each bracketed by CUDA
+events on the launching stream, with L2 flushed before every step by writing
+a 256 MiB buffer (the workloads' inputs and outputs are smaller than L2).  The
+timed region is bracketed by a barrier and a device synchronise on both sides;
+the reported time is the max over ranks.
+
+``--impl reference`` times the CPU oracle as it stands (fp64 C, OpenMP over the
+host cores) on a bounded sample of the same workload, extrapolated to the full
+workload by rows.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sdpa_forward_materialised_gb300 import workloads as W  # noqa: E402
+
+METRIC = "(O,P) fwd ms, TFLOPS and HBM GB/s; % of roofline (1×GB300)"
+FLUSH_BYTES = 256 << 20
+# Pages' own number for the default workload (Ascend 910, Triton, fp16): context only.
+PAGES_MS = {"prefill1k_d64_f16": 0.515, "prefill2k_d128_f16": 1.369, "gqa1k_d128_f16": 0.810,
+            "tail100_mask_f16": 0.219}
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def elem(dtype) -> int:
+    return torch.empty((), dtype=dtype).element_size()
+
+
+def algorithmic_bytes(w: W.Workload) -> int:
+    """Q, K, V read once, mask read once at its broadcast shape, O and the full P written."""
+    e = elem(w.torch_dtype)
+    q = w.B * w.Hq * w.Sq * w.D * e
+    kv = 2 * w.B * w.Hkv * w.Skv * w.D * e
+    o = w.B * w.Hq * w.Sq * w.D * e
+    p = w.B * w.Hq * w.Sq * w.Skv * e
+    m = w.B * 1 * w.Sq * w.Skv if w.mask else 0
+    return q + kv + o + p + m
+
+
+def live_scores(w: W.Workload) -> int:
+    per = 0
+    for i in range(w.Sq):
+        per += min(i + 1, w.Skv) if w.is_causal else w.Skv
+    return w.B * w.Hq * per
+
+
+def flops(w: W.Workload):
+    """(algorithmic, dense) FLOPs: QK^T and PV, 2 per MAC; algorithmic counts
+    live (causally visible) scores only, dense counts every score (the pages'
+    TFLOPS convention)."""
+    alg = 4 * w.D * live_scores(w)
+    dense = 4 * w.D * w.B * w.Hq * w.Sq * w.Skv
+    return alg, dense
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        use = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:1]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_region": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm_mhz, max_mhz = [], []
+        for _, p in use:
+            try:
+                sm_mhz.append(float(p[1]))
+                max_mhz.append(float(p[2]))
+            except ValueError:
+                pass
+            for n, val in zip(names, p[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm_mhz) if sm_mhz else None,
+                "sm_max_mhz": max(max_mhz) if max_mhz else None,
+                "reasons": sorted(reasons), "samples_in_region": len(inside)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(backend: str):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_ms(w: W.Workload, budget_s: float, inputs=None):
+    """Time the oracle on a row sample sized for ~budget_s; return
+    (ms extrapolated to the full workload, threads, sample description)."""
+    import numpy as np
+    import oracle
+    q, k, v, m = inputs if inputs is not None else W.make_inputs(w)
+    threads = max(1, os.cpu_count() or 1)
+    total = w.B * w.Hq * w.Sq
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(total, size=min(total, max(threads * 2, 16)), replace=False))
+    t0 = time.perf_counter()
+    oracle.oracle_fwd(q, k, v, m, is_causal=w.is_causal, scale=w.scale, rows=probe, nthreads=threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    n = int(min(total, max(len(probe), budget_s / max(per_row, 1e-9))))
+    rows = np.sort(rng.choice(total, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.oracle_fwd(q, k, v, m, is_causal=w.is_causal, scale=w.scale, rows=rows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 * total / n
+    sample = (f"{n} of {total} query rows (each over all {w.Skv} keys), fp64 C oracle, "
+              f"{threads} OpenMP threads, {dt:.2f} s, extrapolated to all rows")
+    return ms, threads, sample
+
+
+def run_reference(args, w: W.Workload):
+    world, rank, _ = dist_setup("gloo")
+    if rank != 0:
+        return 0
+    inputs = W.make_inputs(w)
+    per_step = max(0.5, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample_ms(w, per_step / 4, inputs)
+    vals, threads, sample = [], 1, ""
+    for _ in range(args.steps):
+        ms, threads, sample = oracle_sample_ms(w, per_step, inputs)
+        vals.append(ms)
+    ms = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, **{k: v for k, v in w.describe().items() if k != "name"}},
+        "cpu_baseline": {"value": ms, "unit": "ms", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, w: W.Workload):
+    import sdpa_forward_materialised_gb300 as sm
+    world, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sm.load_library()
+
+    q, k, v, m = W.make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = m.to(dev) if m is not None else None
+    kind = sm.MASK_NONE if md is None else (sm.MASK_BOOL if md.dtype == torch.bool else sm.MASK_ADDITIVE)
+    O, P = sm.empty_outputs(qd, vd, w.Skv)
+    plan = sm.sdpa_math_plan(qd, kd, vd, md, is_causal=w.is_causal, scale=w.scale, out=O, probs=P,
+                             variant=args.variant)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        sm.sdpa_math_fwd_ex(qd, kd, vd, md, kind, w.is_causal, w.scale, O, P, None, args.variant, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    sm.sdpa_math_device_status(stream)
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t1 = time.perf_counter()
+    time.sleep(0.15)
+    sampler.stop()
+    sm.sdpa_math_device_status(stream)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    clocks = sampler.summary(t0, t1)
+
+    # end to end through the same C-ABI call, host buffers in pinned memory
+    hq, hk, hv = q.pin_memory(), k.pin_memory(), v.pin_memory()
+    hm = m.pin_memory() if m is not None else None
+    hO = torch.empty(O.shape, dtype=O.dtype).pin_memory()
+    hP = torch.empty(P.shape, dtype=P.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hm,) if hm is not None else ()))
+    d2h = hO.numel() * hO.element_size() + hP.numel() * hP.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        qd.copy_(hq, non_blocking=True)
+        kd.copy_(hk, non_blocking=True)
+        vd.copy_(hv, non_blocking=True)
+        if hm is not None:
+            md.copy_(hm, non_blocking=True)
+        step()
+        hO.copy_(O, non_blocking=True)
+        hP.copy_(P, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(es.elapsed_time(ee) / e2e_steps, world, dev)
+
+    peaks, peak_src = load_peaks()
+    nbytes = algorithmic_bytes(w)
+    alg, dense = flops(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    traffic = ncu_traffic(w, plan["variant"])
+    line = {
+        "metric": METRIC, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": (ms / PAGES_MS[w.name]) if w.name in PAGES_MS else None,
+        "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv,
+                   "D": w.D, "is_causal": w.is_causal, "mask": w.mask, "seed": w.seed,
+                   "variant": plan["variant"], "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "vs_baseline_ref": "Ascend 910 Triton ms from the pages (other hardware, context only)"},
+        "tflops_alg": alg / (ms * 1e-3) / 1e12, "tflops_dense": dense / (ms * 1e-3) / 1e12,
+        "hbm_gbs": gbs, "algorithmic_bytes": nbytes,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} (copy bandwidth, burst)"},
+        "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * plan["launches"],
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cms, threads, sample = oracle_sample_ms(w, args.cpu_budget, (q, k, v, m))
+        line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def ncu_traffic(w: W.Workload, variant: str):
+    """DRAM bytes per launch from the committed ncu summary, only when it was
+    taken on the kernel sources as they are now (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        from sdpa_forward_materialised_gb300 import _build
+        fp = _build.source_fingerprint()
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(w.name)
+        if ent and ent.get("sources") == fp and ent.get("variant") == variant:
+            return ent["dram_bytes_per_launch"]
+    except Exception:
+        return None
+    return None
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="prefill1k_d64_f16", choices=sorted(W.BY_NAME))
+    ap.add_argument("--variant", default="auto", choices=["auto", "simt", "twopass", "fused", "decode"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
+    w = W.BY_NAME[args.config]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

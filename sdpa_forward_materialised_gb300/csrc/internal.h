@@ -1,0 +1,57 @@
+// internal.h -- validated problem descriptor shared by the host API and the
+// kernel launchers of the materialised-probability SDPA forward.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sdpa {
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2, kBool = 3 };
+enum MaskKind : int { kMaskNone = 0, kMaskBool = 1, kMaskAdditive = 2 };
+
+// Everything a kernel needs, after host validation.  Strides are in elements;
+// a broadcast mask extent has stride 0.  Rows are indexed (b, h, i) with the
+// key/value head of query head h equal to h / group.
+struct Problem {
+    int dtype;  // DType of q, k, v, out, probs
+    int64_t B, Hq, Hkv, Sq, Skv, D, Dv, group;
+    const void* q;  int64_t sq[4];
+    const void* k;  int64_t sk[4];
+    const void* v;  int64_t sv[4];
+    const void* mask; int mask_kind; int mask_dtype; int64_t sm[4];
+    int causal;
+    float scale;
+    void* o;  int64_t so[4];
+    void* p;  int64_t sp[4];
+    float* lse;  // optional [B, Hq, Sq] contiguous, natural-log LSE
+};
+
+// Number of 128x128 score tiles that survive top-left causal truncation for
+// one (b, h) slice.
+inline int64_t live_tiles_per_slice(int64_t Sq, int64_t Skv, bool causal) {
+    const int64_t tq = (Sq + 127) / 128, tk = (Skv + 127) / 128;
+    if (!causal) return tq * tk;
+    int64_t n = 0;
+    for (int64_t t = 0; t < tq; ++t) {
+        const int64_t last_row = (t + 1) * 128 - 1 < Sq - 1 ? (t + 1) * 128 - 1 : Sq - 1;
+        const int64_t keys = last_row + 1 < Skv ? last_row + 1 : Skv;
+        n += (keys + 127) / 128;
+    }
+    return n;
+}
+
+// Kernel launchers.  Each returns cudaSuccess or the launch error.  `why`
+// receives a static reason string when a launcher cannot serve the problem
+// (then it returns cudaErrorNotSupported without launching).
+cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
+bool tc_supports(const Problem& p, bool fused, const char** why);
+cudaError_t launch_tc(const Problem& p, bool fused, cudaStream_t stream);
+bool decode_supports(const Problem& p, const char** why);
+cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+
+// Device error word shared by every kernel of the library (see
+// sdpa_math_device_status).  read_and_clear returns the word's old value.
+cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int* value);
+
+}  // namespace sdpa

@@ -1,0 +1,305 @@
+// sdpa_api.cu -- host side of the C ABI declared in include/sdpa_math.h:
+// argument validation (before any launch), kernel-family selection by counted
+// live score tiles, and dispatch to the launchers.
+//
+// Semantics enforced here follow FlagOS-OP PR #10 "feat: add sdpa_math
+// operator" (overview, "semantics" item): causal and attn_mask are mutually
+// exclusive, GQA needs Hq % Hkv == 0, dropout is not part of the call; the
+// "_d1()" micro-optimisation item (2026-10-02 update) fixes the layout rule
+// that only the innermost stride must be 1.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "../../include/sdpa_math.h"
+#include "internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sdpa_status fail(sdpa_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+// SDPA_MATH_VARIANT=auto|simt|twopass|fused|decode, read once at load.
+sdpa_variant env_variant() {
+    static const sdpa_variant v = [] {
+        const char* e = std::getenv("SDPA_MATH_VARIANT");
+        if (!e || !*e || !std::strcmp(e, "auto")) return SDPA_VARIANT_AUTO;
+        if (!std::strcmp(e, "simt")) return SDPA_VARIANT_SIMT;
+        if (!std::strcmp(e, "twopass")) return SDPA_VARIANT_TC_TWOPASS;
+        if (!std::strcmp(e, "fused")) return SDPA_VARIANT_TC_FUSED;
+        if (!std::strcmp(e, "decode")) return SDPA_VARIANT_DECODE;
+        return SDPA_VARIANT_AUTO;
+    }();
+    return v;
+}
+
+int64_t elem_size(int dt) {
+    switch (dt) {
+        case SDPA_F32: return 4;
+        case SDPA_F16: case SDPA_BF16: return 2;
+        case SDPA_BOOL: return 1;
+        default: return 0;
+    }
+}
+
+const char* dtype_name(int dt) {
+    switch (dt) {
+        case SDPA_F32: return "f32";
+        case SDPA_F16: return "f16";
+        case SDPA_BF16: return "bf16";
+        case SDPA_BOOL: return "bool";
+        default: return "unknown";
+    }
+}
+
+int64_t numel(const sdpa_tensor* t) {
+    int64_t n = 1;
+    for (int i = 0; i < 4; ++i) n *= t->shape[i];
+    return n;
+}
+
+// Checks shared by every tensor argument.
+sdpa_status check_tensor(const sdpa_tensor* t, const char* name) {
+    if (!t) return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: tensor descriptor is NULL", name);
+    for (int i = 0; i < 4; ++i) {
+        if (t->shape[i] < 0)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: negative extent shape[%d]=%lld", name, i,
+                        (long long)t->shape[i]);
+        if (t->stride[i] < 0)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: negative stride[%d]", name, i);
+    }
+    const int64_t es = elem_size(t->dtype);
+    if (es == 0) return fail(SDPA_ERR_UNSUPPORTED, "%s: unknown dtype %d", name, (int)t->dtype);
+    if (numel(t) > 0) {
+        if (!t->data) return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: data pointer is NULL", name);
+        if (((uintptr_t)t->data) % (uintptr_t)es != 0)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: data pointer not aligned to its %lld-byte element",
+                        name, (long long)es);
+        if (t->shape[3] > 1 && t->stride[3] != 1)
+            return fail(SDPA_ERR_INVALID_ARGUMENT,
+                        "%s: innermost stride must be 1 (got %lld)", name, (long long)t->stride[3]);
+    }
+    return SDPA_OK;
+}
+
+bool same_shape(const sdpa_tensor* t, int64_t a, int64_t b, int64_t c, int64_t d) {
+    return t->shape[0] == a && t->shape[1] == b && t->shape[2] == c && t->shape[3] == d;
+}
+
+// Full validation; fills `p` on success.
+sdpa_status validate(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                     const sdpa_tensor* mask, sdpa_mask_kind mask_kind, int is_causal, float scale,
+                     const sdpa_tensor* out, const sdpa_tensor* probs, sdpa::Problem* p) {
+    sdpa_status s;
+    if ((s = check_tensor(q, "q")) != SDPA_OK) return s;
+    if ((s = check_tensor(k, "k")) != SDPA_OK) return s;
+    if ((s = check_tensor(v, "v")) != SDPA_OK) return s;
+    if ((s = check_tensor(out, "out")) != SDPA_OK) return s;
+    if ((s = check_tensor(probs, "probs")) != SDPA_OK) return s;
+
+    if (q->dtype != SDPA_F32 && q->dtype != SDPA_F16 && q->dtype != SDPA_BF16)
+        return fail(SDPA_ERR_UNSUPPORTED, "q: dtype %s is not f32/f16/bf16", dtype_name(q->dtype));
+    const sdpa_tensor* same[] = {k, v, out, probs};
+    const char* names[] = {"k", "v", "out", "probs"};
+    for (int i = 0; i < 4; ++i)
+        if (same[i]->dtype != q->dtype)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: dtype %s differs from q dtype %s", names[i],
+                        dtype_name(same[i]->dtype), dtype_name(q->dtype));
+
+    const int64_t B = q->shape[0], Hq = q->shape[1], Sq = q->shape[2], D = q->shape[3];
+    const int64_t Hkv = k->shape[1], Skv = k->shape[2], Dv = v->shape[3];
+    if (k->shape[0] != B || v->shape[0] != B)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "batch mismatch: q %lld, k %lld, v %lld", (long long)B,
+                    (long long)k->shape[0], (long long)v->shape[0]);
+    if (v->shape[1] != Hkv)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "k and v disagree on heads (%lld vs %lld)",
+                    (long long)Hkv, (long long)v->shape[1]);
+    if (v->shape[2] != Skv)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "k and v disagree on key length (%lld vs %lld)",
+                    (long long)Skv, (long long)v->shape[2]);
+    if (k->shape[3] != D)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "q and k disagree on head dim (%lld vs %lld)",
+                    (long long)D, (long long)k->shape[3]);
+    if (Hkv == 0 ? Hq != 0 : (Hq % Hkv) != 0)
+        return fail(SDPA_ERR_INVALID_ARGUMENT,
+                    "GQA requires Hq divisible by Hkv (Hq=%lld, Hkv=%lld)", (long long)Hq,
+                    (long long)Hkv);
+    if (is_causal && mask_kind != SDPA_MASK_NONE)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "is_causal and an attention mask are mutually exclusive");
+    if (!std::isfinite(scale)) return fail(SDPA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    if (D > 256 || Dv > 256)
+        return fail(SDPA_ERR_UNSUPPORTED, "head dim above 256 is not supported (D=%lld, Dv=%lld)",
+                    (long long)D, (long long)Dv);
+    if (!same_shape(out, B, Hq, Sq, Dv))
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "out must be [B,Hq,Sq,Dv] = [%lld,%lld,%lld,%lld]",
+                    (long long)B, (long long)Hq, (long long)Sq, (long long)Dv);
+    if (!same_shape(probs, B, Hq, Sq, Skv))
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "probs must be [B,Hq,Sq,Skv] = [%lld,%lld,%lld,%lld]",
+                    (long long)B, (long long)Hq, (long long)Sq, (long long)Skv);
+
+    std::memset(p, 0, sizeof(*p));
+    if (mask_kind == SDPA_MASK_NONE) {
+        if (mask) return fail(SDPA_ERR_INVALID_ARGUMENT, "mask given with mask_kind NONE");
+    } else if (mask_kind == SDPA_MASK_BOOL || mask_kind == SDPA_MASK_ADDITIVE) {
+        if (!mask) return fail(SDPA_ERR_INVALID_ARGUMENT, "mask_kind set but mask is NULL");
+        if ((s = check_tensor(mask, "mask")) != SDPA_OK) return s;
+        const int64_t mb = mask->shape[0], mh = mask->shape[1];
+        if (!(mb == 1 || mb == B) || !(mh == 1 || mh == Hq) || mask->shape[2] != Sq ||
+            mask->shape[3] != Skv)
+            return fail(SDPA_ERR_INVALID_ARGUMENT,
+                        "mask shape must be [1|B, 1|Hq, Sq, Skv] = [1|%lld, 1|%lld, %lld, %lld]",
+                        (long long)B, (long long)Hq, (long long)Sq, (long long)Skv);
+        if (mask_kind == SDPA_MASK_BOOL && mask->dtype != SDPA_BOOL)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "a bool mask must have dtype bool");
+        if (mask_kind == SDPA_MASK_ADDITIVE && mask->dtype != q->dtype && mask->dtype != SDPA_F32)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "an additive mask must have the q dtype or f32");
+        p->mask = mask->data;
+        p->mask_kind = mask_kind;
+        p->mask_dtype = mask->dtype;
+        p->sm[0] = (mb == 1) ? 0 : mask->stride[0];
+        p->sm[1] = (mh == 1) ? 0 : mask->stride[1];
+        p->sm[2] = mask->stride[2];
+        p->sm[3] = 1;
+    } else {
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "unknown mask_kind %d", (int)mask_kind);
+    }
+
+    p->dtype = q->dtype;
+    p->B = B; p->Hq = Hq; p->Hkv = Hkv; p->Sq = Sq; p->Skv = Skv; p->D = D; p->Dv = Dv;
+    p->group = Hkv > 0 ? Hq / Hkv : 1;
+    p->q = q->data; p->k = k->data; p->v = v->data; p->o = out->data; p->p = probs->data;
+    for (int i = 0; i < 4; ++i) {
+        p->sq[i] = q->stride[i]; p->sk[i] = k->stride[i]; p->sv[i] = v->stride[i];
+        p->so[i] = out->stride[i]; p->sp[i] = probs->stride[i];
+    }
+    p->sq[3] = p->sk[3] = p->sv[3] = p->so[3] = p->sp[3] = 1;
+    p->causal = is_causal ? 1 : 0;
+    p->scale = scale;
+    p->lse = nullptr;
+    return SDPA_OK;
+}
+
+// Live-tile threshold below which the single-sweep fused tensor-core kernel is
+// used (score row blocks of at most 512 keys fit the 512 TMEM columns).
+constexpr int64_t kFusedMaxKeys = 512;
+
+// Variant the AUTO rule picks for a validated problem.
+sdpa_variant choose(const sdpa::Problem& p) {
+    const char* why = nullptr;
+    if (p.dtype == SDPA_F32) return SDPA_VARIANT_SIMT;
+    if (sdpa::decode_supports(p, &why)) return SDPA_VARIANT_DECODE;
+    if (p.Skv <= kFusedMaxKeys && sdpa::tc_supports(p, true, &why)) return SDPA_VARIANT_TC_FUSED;
+    if (sdpa::tc_supports(p, false, &why)) return SDPA_VARIANT_TC_TWOPASS;
+    return SDPA_VARIANT_SIMT;
+}
+
+sdpa_status resolve(const sdpa::Problem& p, sdpa_variant requested, sdpa_variant* out) {
+    sdpa_variant v = requested == SDPA_VARIANT_AUTO ? env_variant() : requested;
+    const char* why = "not supported";
+    switch (v) {
+        case SDPA_VARIANT_AUTO: *out = choose(p); return SDPA_OK;
+        case SDPA_VARIANT_SIMT: *out = v; return SDPA_OK;
+        case SDPA_VARIANT_TC_TWOPASS:
+        case SDPA_VARIANT_TC_FUSED:
+            if (!sdpa::tc_supports(p, v == SDPA_VARIANT_TC_FUSED, &why))
+                return fail(SDPA_ERR_UNSUPPORTED, "tensor-core variant cannot serve this call: %s", why);
+            *out = v;
+            return SDPA_OK;
+        case SDPA_VARIANT_DECODE:
+            if (!sdpa::decode_supports(p, &why))
+                return fail(SDPA_ERR_UNSUPPORTED, "decode variant cannot serve this call: %s", why);
+            *out = v;
+            return SDPA_OK;
+        default:
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "unknown variant %d", (int)v);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sdpa_math_last_error(void) { return g_last_error.c_str(); }
+
+int sdpa_math_abi_version(void) { return SDPA_MATH_ABI_VERSION; }
+
+sdpa_status sdpa_math_plan(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                           const sdpa_tensor* mask, sdpa_mask_kind mask_kind, int is_causal,
+                           float scale, const sdpa_tensor* out, const sdpa_tensor* probs,
+                           sdpa_variant requested, sdpa_plan* plan) {
+    g_last_error.clear();
+    if (!plan) return fail(SDPA_ERR_INVALID_ARGUMENT, "plan is NULL");
+    sdpa::Problem p;
+    sdpa_status s = validate(q, k, v, mask, mask_kind, is_causal, scale, out, probs, &p);
+    if (s != SDPA_OK) return s;
+    sdpa_variant chosen;
+    if ((s = resolve(p, requested, &chosen)) != SDPA_OK) return s;
+    plan->variant = chosen;
+    plan->live_score_tiles = p.B * p.Hq * sdpa::live_tiles_per_slice(p.Sq, p.Skv, p.causal != 0);
+    plan->launches = (p.B * p.Hq * p.Sq == 0) ? 0 : 1;
+    return SDPA_OK;
+}
+
+sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                             const sdpa_tensor* mask, sdpa_mask_kind mask_kind, int is_causal,
+                             float scale, sdpa_tensor* out, sdpa_tensor* probs, float* lse,
+                             sdpa_variant variant, sdpa_stream_t stream) {
+    g_last_error.clear();
+    sdpa::Problem p;
+    sdpa_status s = validate(q, k, v, mask, mask_kind, is_causal, scale, out, probs, &p);
+    if (s != SDPA_OK) return s;
+    if (lse && ((uintptr_t)lse) % 4 != 0)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "lse pointer not 4-byte aligned");
+    p.lse = lse;
+    sdpa_variant chosen;
+    if ((s = resolve(p, variant, &chosen)) != SDPA_OK) return s;
+    if (p.B * p.Hq * p.Sq == 0) return SDPA_OK;  // nothing to write
+
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    switch (chosen) {
+        case SDPA_VARIANT_TC_TWOPASS: e = sdpa::launch_tc(p, false, st); break;
+        case SDPA_VARIANT_TC_FUSED: e = sdpa::launch_tc(p, true, st); break;
+        case SDPA_VARIANT_DECODE: e = sdpa::launch_decode(p, st); break;
+        default: e = sdpa::launch_simt(p, st); break;
+    }
+    if (e != cudaSuccess)
+        return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SDPA_OK;
+}
+
+sdpa_status sdpa_math_fwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                          const sdpa_tensor* mask, sdpa_mask_kind mask_kind, int is_causal,
+                          float scale, sdpa_tensor* out, sdpa_tensor* probs, sdpa_stream_t stream) {
+    return sdpa_math_fwd_ex(q, k, v, mask, mask_kind, is_causal, scale, out, probs, nullptr,
+                            SDPA_VARIANT_AUTO, stream);
+}
+
+sdpa_status sdpa_math_device_status(sdpa_stream_t stream) {
+    g_last_error.clear();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "stream synchronize failed: %s", cudaGetErrorString(e));
+    unsigned int word = 0;
+    e = sdpa::status_read_and_clear(st, &word);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "reading the device status failed: %s", cudaGetErrorString(e));
+    if (word != 0)
+        return fail(SDPA_ERR_TIMEOUT,
+                    "a device-side wait ran out of iterations (role %u, barrier %u, block %u)",
+                    (word >> 24) & 0xff, (word >> 16) & 0xff, word & 0xffff);
+    return SDPA_OK;
+}
+
+}  // extern "C"

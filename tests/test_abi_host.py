@@ -1,0 +1,197 @@
+"""C-ABI host checks (no GPU): the library loads, exports every declared
+symbol, and rejects bad arguments on the host before any launch.
+
+Argument rules follow FlagOS-OP PR #10 "feat: add sdpa_math operator"
+(semantics item: causal and mask mutually exclusive, GQA divisibility; the
+"_d1()" micro-optimisation item: only the innermost stride must be 1).
+Valid argument sets are only ever passed to ``sdpa_math_plan``, which never
+touches the GPU.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+import sdpa_forward_materialised_gb300 as sm
+from sdpa_forward_materialised_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sm.load_library()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(sdpa_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert "sdpa_math_fwd" in names and "sdpa_math_last_error" in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_abi_version(lib):
+    assert sm.sdpa_math_abi_version() == 1
+
+
+def _qkv(B=2, Hq=4, Hkv=2, Sq=33, Skv=47, D=64, Dv=None, dtype=torch.float16):
+    Dv = D if Dv is None else Dv
+    return (torch.zeros(B, Hq, Sq, D, dtype=dtype), torch.zeros(B, Hkv, Skv, D, dtype=dtype),
+            torch.zeros(B, Hkv, Skv, Dv, dtype=dtype))
+
+
+def _expect(status_name, fn, match=None):
+    with pytest.raises(sm.SdpaError) as ei:
+        fn()
+    assert sm.STATUS[ei.value.status] == status_name, str(ei.value)
+    if match:
+        assert re.search(match, str(ei.value)), str(ei.value)
+
+
+def test_plan_accepts_valid_calls(lib):
+    q, k, v = _qkv()
+    r = sm.sdpa_math_plan(q, k, v)
+    assert r["launches"] == 1
+    assert r["live_score_tiles"] == 2 * 4 * 1 * 1
+
+
+def test_error_causal_with_mask(lib):
+    q, k, v = _qkv()
+    m = torch.ones(1, 1, 33, 47, dtype=torch.bool)
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v, m, is_causal=True),
+            "mutually exclusive")
+
+
+def test_error_gqa_not_divisible(lib):
+    q, k, v = _qkv(Hq=6, Hkv=4)
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v), "divisible")
+
+
+def test_error_dtype_mismatch(lib):
+    q, k, v = _qkv()
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k.float(), v), "dtype")
+
+
+def test_error_unsupported_dtype_and_head_dim(lib):
+    q, k, v = _qkv(dtype=torch.float64)
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v))
+    q, k, v = _qkv(D=264)
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v), "256")
+
+
+def test_error_shapes(lib):
+    q, k, v = _qkv()
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k[:1], v), "batch")
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v[:, :, :40]), "key length")
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k[..., :32], v), "head dim")
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v, out_shape=(2, 4, 33, 63)),
+            "out must be")
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v, probs_shape=(2, 4, 33, 46)),
+            "probs must be")
+
+
+def test_error_innermost_stride(lib):
+    q, k, v = _qkv()
+    qt = torch.zeros(2, 4, 64, 33, dtype=torch.float16).transpose(2, 3)  # stride(-1) = 33
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(qt, k, v), "innermost stride")
+    # a transposed [B, S, H, D] layout keeps stride(-1) == 1 and is accepted
+    qs = torch.zeros(2, 33, 4, 64, dtype=torch.float16).transpose(1, 2)
+    assert sm.sdpa_math_plan(qs, k, v)["launches"] == 1
+
+
+def test_error_mask_shape_and_dtype(lib):
+    q, k, v = _qkv()
+    for shape in [(3, 1, 33, 47), (1, 2, 33, 47), (1, 1, 32, 47), (1, 1, 33, 48)]:
+        _expect("SDPA_ERR_INVALID_ARGUMENT",
+                lambda: sm.sdpa_math_plan(q, k, v, torch.ones(shape, dtype=torch.bool)), "mask shape")
+    for shape in [(1, 1, 33, 47), (2, 1, 33, 47), (1, 4, 33, 47), (2, 4, 33, 47)]:
+        assert sm.sdpa_math_plan(q, k, v, torch.ones(shape, dtype=torch.bool))["launches"] == 1
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_plan(q, k, v, torch.ones(1, 1, 33, 47, dtype=torch.bfloat16)),
+            "additive mask")
+    assert sm.sdpa_math_plan(q, k, v, torch.zeros(1, 1, 33, 47, dtype=torch.float32))["launches"] == 1
+
+
+def test_error_scale_not_finite(lib):
+    q, k, v = _qkv()
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v, scale=float("nan")), "finite")
+    _expect("SDPA_ERR_INVALID_ARGUMENT", lambda: sm.sdpa_math_plan(q, k, v, scale=float("inf")), "finite")
+
+
+def test_error_null_and_misaligned_pointers(lib):
+    q, k, v = _qkv()
+    out = torch.empty(2, 4, 33, 64, dtype=torch.float16)
+    probs = torch.empty(2, 4, 33, 47, dtype=torch.float16)
+    dq, dk, dv, do, dp = (sm.describe(t) for t in (q, k, v, out, probs))
+    plan = sm.SdpaPlan()
+    dq.data = None
+    st = lib.sdpa_math_plan(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), None, 0, 0,
+                            ctypes.c_float(0.125), ctypes.byref(do), ctypes.byref(dp), 0,
+                            ctypes.byref(plan))
+    assert st == sm.SDPA_ERR_INVALID_ARGUMENT and b"NULL" in lib.sdpa_math_last_error()
+    dq = sm.describe(q)
+    dq.data = q.data_ptr() + 1
+    st = lib.sdpa_math_plan(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), None, 0, 0,
+                            ctypes.c_float(0.125), ctypes.byref(do), ctypes.byref(dp), 0,
+                            ctypes.byref(plan))
+    assert st == sm.SDPA_ERR_INVALID_ARGUMENT and b"aligned" in lib.sdpa_math_last_error()
+    # the fwd entry point validates the same way before touching CUDA
+    st = lib.sdpa_math_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), None, 0, 0,
+                           ctypes.c_float(0.125), ctypes.byref(do), ctypes.byref(dp), None)
+    assert st == sm.SDPA_ERR_INVALID_ARGUMENT
+    # mask kind without a mask, and a mask with kind NONE
+    dq = sm.describe(q)
+    st = lib.sdpa_math_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), None, 1, 0,
+                           ctypes.c_float(0.125), ctypes.byref(do), ctypes.byref(dp), None)
+    assert st == sm.SDPA_ERR_INVALID_ARGUMENT and b"mask" in lib.sdpa_math_last_error()
+    dm = sm.describe(torch.ones(1, 1, 33, 47, dtype=torch.bool))
+    st = lib.sdpa_math_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(dm), 0, 0,
+                           ctypes.c_float(0.125), ctypes.byref(do), ctypes.byref(dp), None)
+    assert st == sm.SDPA_ERR_INVALID_ARGUMENT
+
+
+def test_dropout_rejected_by_binding():
+    q, k, v = _qkv()
+    with pytest.raises(ValueError, match="dropout"):
+        sm.sdpa_math(q, k, v, dropout_p=0.1)
+
+
+def test_last_error_is_cleared_on_success(lib):
+    q, k, v = _qkv(Hq=6, Hkv=4)
+    with pytest.raises(sm.SdpaError):
+        sm.sdpa_math_plan(q, k, v)
+    assert sm.sdpa_math_last_error() != ""
+    q, k, v = _qkv()
+    sm.sdpa_math_plan(q, k, v)
+    assert sm.sdpa_math_last_error() == ""
+
+
+@pytest.mark.parametrize("Sq,Skv,causal,expect", [
+    (1024, 1024, True, 36), (2048, 2048, True, 136), (1024, 1024, False, 64),
+    (100, 100, False, 1), (1, 1152, False, 9), (512, 512, True, 10), (128, 2048, False, 16),
+    (0, 5, False, 0), (130, 300, True, 3)])
+def test_live_tile_count(lib, Sq, Skv, causal, expect):
+    """Live 128x128 score tiles after top-left causal truncation, per (b, h)."""
+    q, k, v = _qkv(B=1, Hq=1, Hkv=1, Sq=Sq, Skv=Skv, D=8)
+    assert sm.sdpa_math_plan(q, k, v, is_causal=causal)["live_score_tiles"] == expect
+
+
+def test_f32_always_plans_simt(lib):
+    q, k, v = _qkv(dtype=torch.float32)
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "simt"

@@ -1,0 +1,210 @@
+"""GPU-vs-oracle parity of the (O, P) forward, through the C ABI.
+
+Every case draws seeded inputs once, runs the CUDA path (outputs pre-filled
+with NaN so an unwritten element cannot pass) and compares with the fp64 CPU
+oracle element by element: in full at sizes the oracle finishes in seconds
+(several tiles plus a ragged tail), and on sampled rows at the benchmark
+shapes, together with properties that hold at any size (row sums, the zero
+causal triangle, zero fully masked rows).
+
+Semantics: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- (out, P) of the
+SDPA math backend; causal and mask mutually exclusive; bool mask = -inf
+masking; fully masked row -> P = O = 0; GQA with Hq % Hkv == 0.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import sdpa_forward_materialised_gb300 as sm
+from sdpa_forward_materialised_gb300 import workloads as W
+from oracle import oracle_fwd
+from parity_util import compare, row_sum_bound, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+NTHREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    sm.load_library()
+
+
+def _run(q, k, v, mask, causal, scale, variant="auto", lse=False):
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = mask.to(dev) if mask is not None else None
+    if md is not None:
+        while md.dim() < 4:
+            md = md.unsqueeze(0)
+    B, Hq, Sq, _ = q.shape
+    Skv, Dv = k.shape[2], v.shape[3]
+    O = torch.full((B, Hq, Sq, Dv), float("nan"), dtype=q.dtype, device=dev)
+    P = torch.full((B, Hq, Sq, Skv), float("nan"), dtype=q.dtype, device=dev)
+    L = torch.full((B, Hq, Sq), float("nan"), dtype=torch.float32, device=dev) if lse else None
+    kind = sm.MASK_NONE if md is None else (sm.MASK_BOOL if md.dtype == torch.bool else sm.MASK_ADDITIVE)
+    sm.sdpa_math_fwd_ex(qd, kd, vd, md, kind, causal, scale, O, P, L, variant)
+    torch.cuda.synchronize()
+    sm.sdpa_math_device_status()
+    return O, P, L
+
+
+def _full_check(q, k, v, mask, causal, scale, variant="auto", check_lse=True):
+    O, P, L = _run(q, k, v, mask, causal, scale, variant, lse=check_lse)
+    Or, Pr, lr = oracle_fwd(q, k, v, mask, is_causal=causal, scale=scale, nthreads=NTHREADS)
+    so = compare(O, Or, q.dtype, "O")
+    sp = compare(P, Pr, q.dtype, "P")
+    if check_lse:
+        Lg = L.double().cpu().numpy()
+        dead = np.isneginf(lr)
+        assert np.all(np.isneginf(Lg[dead])), "LSE of fully masked rows must be -inf"
+        np.testing.assert_allclose(Lg[~dead], lr[~dead], rtol=2e-6, atol=2e-5)
+    return so, sp
+
+
+def _variants_for(q, k, v, mask, causal):
+    """Every kernel family that accepts this call (the SIMT one always does)."""
+    out = []
+    for name in ("simt", "twopass", "fused", "decode"):
+        try:
+            sm.sdpa_math_plan(q, k, v, mask, is_causal=causal, variant=name)
+            out.append(name)
+        except sm.SdpaError:
+            pass
+    return out
+
+
+# --------------------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("w", [W.TINY, W.TAIL100, W.DECODE], ids=lambda w: w.name)
+def test_workload_full_compare(w):
+    q, k, v, m = W.make_inputs(w)
+    for variant in ["auto"] + _variants_for(q, k, v, m, w.is_causal):
+        _full_check(q, k, v, m, w.is_causal, w.scale, variant)
+
+
+@pytest.mark.parametrize("w", [W.PREFILL_1K_D64, W.PREFILL_2K_D128, W.PREFILL_2K_D128_BF16, W.GQA_1K_D128],
+                         ids=lambda w: w.name)
+def test_workload_sampled_rows_and_properties(w):
+    """Full benchmark shape in the benchmark's launch configuration (auto)."""
+    q, k, v, m = W.make_inputs(w)
+    O, P, L = _run(q, k, v, m, w.is_causal, w.scale, "auto", lse=True)
+    rows = sample_rows(w.B, w.Hq, w.Sq, n_random=192, seed=w.seed)
+    Or, Pr, lr = oracle_fwd(q, k, v, m, is_causal=w.is_causal, scale=w.scale, rows=rows, nthreads=NTHREADS)
+    compare(O.reshape(-1, w.D)[torch.from_numpy(rows).cuda()], Or, q.dtype, "O rows")
+    compare(P.reshape(-1, w.Skv)[torch.from_numpy(rows).cuda()], Pr, q.dtype, "P rows")
+    np.testing.assert_allclose(L.reshape(-1)[torch.from_numpy(rows).cuda()].double().cpu().numpy(), lr,
+                               rtol=2e-6, atol=2e-5)
+    # properties over every row
+    assert not torch.isnan(P).any() and not torch.isnan(O).any()
+    sums = P.double().sum(-1)
+    assert (sums - 1).abs().max().item() <= row_sum_bound(q.dtype, w.Skv)
+    assert (P >= 0).all()
+    if w.is_causal:
+        upper = torch.triu(torch.ones(w.Sq, w.Skv, dtype=torch.bool, device=P.device), diagonal=1)
+        assert (P[..., upper] == 0).all()
+
+
+# --------------------------------------------------------------------------- small multi-tile cases
+
+SMALL = [
+    # B, Hq, Hkv, Sq, Skv, D, dtype, causal, mask
+    (1, 2, 2, 300, 300, 64, "f16", True, None),
+    (2, 4, 2, 257, 390, 128, "f16", False, None),
+    (1, 8, 2, 200, 136, 128, "bf16", False, None),
+    (1, 2, 1, 384, 384, 128, "bf16", True, None),
+    (2, 2, 2, 130, 270, 64, "f16", False, "bool"),
+    (1, 4, 4, 96, 200, 64, "bf16", False, "additive"),
+    (1, 2, 2, 77, 93, 32, "f32", True, None),
+    (2, 3, 3, 50, 61, 96, "f32", False, "bool"),
+    (1, 4, 1, 1, 700, 128, "f16", False, None),
+    (3, 8, 2, 2, 1000, 64, "bf16", False, None),
+    (1, 2, 2, 640, 640, 64, "f16", False, None),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(SMALL)), ids=lambda i: "x".join(str(x) for x in SMALL[i]))
+def test_small_cases_every_variant(idx):
+    B, Hq, Hkv, Sq, Skv, D, dt, causal, mask = SMALL[idx]
+    q, k, v, m = W.make_custom(100 + idx, B, Hq, Hkv, Sq, Skv, D, dt, mask=mask)
+    scale = 1.0 / math.sqrt(D)
+    variants = _variants_for(q, k, v, m, causal)
+    assert "simt" in variants
+    for variant in variants:
+        _full_check(q, k, v, m, causal, scale, variant)
+
+
+# --------------------------------------------------------------------------- edge cases
+
+def test_empty_query_is_a_noop():
+    q, k, v, _ = W.make_custom(1, 1, 2, 2, 0, 16, 64, "f16")
+    O, P, _ = _run(q, k, v, None, False, 0.125)
+    assert O.numel() == 0 and P.numel() == 0
+
+
+def test_zero_keys_give_zero_output():
+    q, k, v, _ = W.make_custom(2, 1, 2, 2, 5, 0, 64, "f16")
+    O, P, L = _run(q, k, v, None, False, 0.125, lse=True)
+    assert (O == 0).all() and P.numel() == 0 and torch.isneginf(L).all()
+
+
+@pytest.mark.parametrize("D,Dv", [(1, 1), (8, 24), (80, 80), (256, 256), (40, 200)])
+def test_head_dims(D, Dv):
+    q, k, v, _ = W.make_custom(3, 1, 2, 2, 70, 90, D, "f16", Dv=Dv)
+    _full_check(q, k, v, None, True, 1.0 / math.sqrt(D))
+
+
+def test_transposed_bshd_layout():
+    """[B,S,H,D] storage viewed as [B,H,S,D] (stride(-1) == 1, no copy)."""
+    q, k, v, _ = W.make_custom(4, 2, 4, 2, 150, 170, 64, "f16")
+    qt = q.transpose(1, 2).contiguous().transpose(1, 2)
+    kt = k.transpose(1, 2).contiguous().transpose(1, 2)
+    vt = v.transpose(1, 2).contiguous().transpose(1, 2)
+    assert not qt.is_contiguous()
+    O, P, _ = _run(qt, kt, vt, None, False, 0.125)
+    Or, Pr, _ = oracle_fwd(q, k, v, None, scale=0.125, nthreads=NTHREADS)
+    compare(O, Or, q.dtype, "O")
+    compare(P, Pr, q.dtype, "P")
+
+
+@pytest.mark.parametrize("mshape", [(1, 1), (2, 1), (1, 4), (2, 4)])
+def test_mask_broadcast_forms(mshape):
+    q, k, v, _ = W.make_custom(5, 2, 4, 2, 40, 72, 64, "f16")
+    g = torch.Generator().manual_seed(9)
+    m = torch.rand(mshape[0], mshape[1], 40, 72, generator=g) < 0.6
+    m[0, 0, 3] = False  # a fully masked row
+    _full_check(q, k, v, m, False, 0.125)
+
+
+def test_additive_mask_f32_and_neg_inf_rows():
+    q, k, v, _ = W.make_custom(6, 1, 2, 2, 33, 65, 64, "bf16")
+    g = torch.Generator().manual_seed(10)
+    m = torch.randn(1, 2, 33, 65, generator=g, dtype=torch.float32)
+    m[0, 1, 7] = float("-inf")
+    m[0, 0, 2, :10] = float("-inf")
+    _full_check(q, k, v, m, False, 0.2)
+
+
+def test_all_rows_masked():
+    q, k, v, _ = W.make_custom(7, 1, 2, 2, 20, 30, 64, "f16")
+    m = torch.zeros(1, 1, 20, 30, dtype=torch.bool)
+    O, P, L = _run(q, k, v, m, False, 0.125, lse=True)
+    assert (O == 0).all() and (P == 0).all() and torch.isneginf(L).all()
+
+
+def test_sdpa_math_wrapper_matches_direct_call():
+    q, k, v, _ = W.make_custom(8, 1, 4, 2, 100, 120, 64, "f16")
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    O, P = sm.sdpa_math(qd, kd, vd, is_causal=True)
+    O2, P2, _ = _run(q, k, v, None, True, 0.125)
+    assert torch.equal(O, O2) and torch.equal(P, P2)
+
+
+def test_forced_unsupported_variant_is_an_error():
+    q, k, v, _ = W.make_custom(9, 1, 2, 2, 16, 16, 64, "f32")
+    with pytest.raises(sm.SdpaError) as ei:
+        _run(q, k, v, None, False, 0.125, variant="twopass")
+    assert ei.value.status == sm.SDPA_ERR_UNSUPPORTED
