@@ -275,6 +275,15 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
         case SDPA_VARIANT_DECODE: e = sdpa::launch_decode(p, st); break;
         default: e = sdpa::launch_simt(p, st); break;
     }
+    // A tensor-core family refuses (before launching anything) when the
+    // driver will not encode a TMA descriptor for this layout; AUTO then
+    // serves the call with the CUDA-core kernel, a forced family reports it.
+    if (e == cudaErrorNotSupported && chosen != SDPA_VARIANT_SIMT) {
+        (void)cudaGetLastError();
+        if (variant != SDPA_VARIANT_AUTO || env_variant() != SDPA_VARIANT_AUTO)
+            return fail(SDPA_ERR_UNSUPPORTED, "the forced kernel family cannot encode TMA descriptors for this layout");
+        e = sdpa::launch_simt(p, st);
+    }
     if (e != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return SDPA_OK;

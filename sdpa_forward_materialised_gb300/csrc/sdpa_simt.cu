@@ -212,7 +212,9 @@ simt_kernel(const Problem p) {
             const T pt = from_f<T>(pr);
             if (rows[r].h >= 0 && j < p.Skv)
                 P[b * p.sp[0] + rows[r].h * p.sp[1] + rows[r].i * p.sp[2] + j] = pt;
-            ps[r * kTileK + c] = (j < p.Skv) ? to_f(pt) : 0.f;
+            // a dead tile skipped the barrier above: other threads may still be
+            // reading ps for the previous tile, and nothing reads it for this one
+            if (live) ps[r * kTileK + c] = (j < p.Skv) ? to_f(pt) : 0.f;
         }
         if (!live) continue;  // the whole tile is above every causal diagonal here
         __syncthreads();

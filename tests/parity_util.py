@@ -3,8 +3,12 @@
 Tolerances (max-abs, on both O and P): f32 1e-5, f16 2e-3, bf16 8e-3.  Where
 the output dtype cannot represent the exact value that closely (bf16 values of
 magnitude >= 4 have a half-ulp of 1.6e-2), an element may instead be off by at
-most one ulp of the dtype at the reference's magnitude; the number of elements
-that needed that allowance is reported.
+most one ulp of the dtype at the reference's magnitude.  For O that allowance
+also carries the rounding of P: the operation returns P in the input dtype and
+O = P V is formed from that rounded P (as the math backend does), so O may
+additionally differ from the exact fp64 value by sum_j half-ulp(P_ij) * |V_j|.
+The number of elements that needed an allowance beyond the plain tolerance
+is reported.
 """
 import numpy as np
 import torch
@@ -22,8 +26,32 @@ def ulp(ref: np.ndarray, dtype) -> np.ndarray:
     return np.ldexp(1.0, (e - MANT[dtype]).astype(np.int64))
 
 
-def compare(got, ref, dtype, what=""):
-    """Element-wise check; returns a stats dict, raises AssertionError on failure."""
+def p_rounding_bound(p_ref: np.ndarray, v_rows: np.ndarray, dtype) -> np.ndarray:
+    """Bound on |O - O_exact| caused by rounding P to ``dtype`` before P V:
+    sum_j (half an ulp of P[i,j]) * |V[j,:]|.  ``p_ref`` is [..., Skv] and
+    ``v_rows`` the matching [..., Skv, Dv] values (already head-mapped)."""
+    half = 0.5 * ulp(p_ref, dtype) * (p_ref != 0)
+    return np.einsum("...j,...je->...e", half, np.abs(v_rows))
+
+
+def o_allowance(p_ref: np.ndarray, v, group: int, dtype, rows=None, Hq=None, Sq=None) -> np.ndarray:
+    """Per-element extra allowance for O (see p_rounding_bound).  Either full
+    [B,Hq,Sq,Skv] references, or flattened ``rows`` with their (Hq, Sq)."""
+    vn = (v.double().numpy() if torch.is_tensor(v) else np.asarray(v, np.float64))
+    if rows is None:
+        vr = np.repeat(vn, group, axis=1)                    # [B,Hq,Skv,Dv]
+        return p_rounding_bound(p_ref, vr[:, :, None, :, :], dtype)
+    b = rows // (Hq * Sq)
+    h = (rows // Sq) % Hq
+    vr = vn[b, h // group]                                   # [n,Skv,Dv]
+    return p_rounding_bound(p_ref, vr, dtype)
+
+
+def compare(got, ref, dtype, what="", extra=None):
+    """Element-wise check; returns a stats dict, raises AssertionError on failure.
+
+    The allowance per element is max(tol, ulp(|ref|) + extra): ``extra`` is
+    the propagated rounding of P for O (``o_allowance``), None for P."""
     g = got.detach().double().cpu().numpy() if torch.is_tensor(got) else np.asarray(got, np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, f"{what}: shape {g.shape} vs {r.shape}"
@@ -32,7 +60,7 @@ def compare(got, ref, dtype, what=""):
     assert not np.isnan(g).any(), f"{what}: NaN in GPU output (unwritten or bad)"
     err = np.abs(g - r)
     tol = TOL[dtype]
-    allow = np.maximum(tol, ulp(r, dtype))
+    allow = np.maximum(tol, ulp(r, dtype) + (0.0 if extra is None else extra))
     bad = err > allow
     if bad.any():
         idx = np.unravel_index(np.argmax(err - allow), err.shape)
