@@ -10,8 +10,11 @@ the shape of the perf-gate baseline of FlagOS-OP PR #10 "feat: add sdpa_math
 operator".  ``--config`` selects another of the synthetic workloads.
 
 Timing: W warm-up steps, then exactly K timed steps, each bracketed by CUDA
-events on the launching stream, with L2 flushed before every step by writing
-a 256 MiB buffer (the workloads' inputs and outputs are smaller than L2).  The
+events on the launching stream.  Before every step L2 is flushed by writing a
+256 MiB buffer and then reading another (the workloads' inputs and outputs
+are smaller than the 129 MB L2, and the read leaves no dirty lines to write
+back during the step), and a ~100 us device sleep keeps the GPU busy while the
+host enqueues the step, so the events time the kernel, not the host call.  The
 timed region is bracketed by a barrier and a device synchronise on both sides;
 the reported time is the max over ranks.
 
@@ -255,12 +258,22 @@ def run_ours(args, w: W.Workload):
                              variant=args.variant)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        # write 256 MiB (evicts the workload from L2), then read another 256 MiB
+        # so the write-back of those dirty lines does not land inside the timed
+        # step; then keep the GPU busy for ~100 us while the host enqueues the
+        # step, so host-side call overhead stays outside the events
+        flush.zero_()
+        flush_rd.sum()
+        torch.cuda._sleep(200_000)
 
     def step():
         sm.sdpa_math_fwd_ex(qd, kd, vd, md, kind, w.is_causal, w.scale, O, P, None, args.variant, stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize(dev)
     sm.sdpa_math_device_status(stream)
@@ -275,7 +288,7 @@ def run_ours(args, w: W.Workload):
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         starts[i].record(stream)
         step()
         ends[i].record(stream)
@@ -334,7 +347,7 @@ def run_ours(args, w: W.Workload):
         "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Skv": w.Skv,
                    "D": w.D, "is_causal": w.is_causal, "mask": w.mask, "seed": w.seed,
-                   "variant": plan["variant"], "l2": "flushed before every step (256 MiB write)",
+                   "variant": plan["variant"], "l2": "flushed before every step (256 MiB write, then 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "vs_baseline_ref": "Ascend 910 Triton ms from the pages (other hardware, context only)"},
         "tflops_alg": alg / (ms * 1e-3) / 1e12, "tflops_dense": dense / (ms * 1e-3) / 1e12,

@@ -1,28 +1,35 @@
 // sdpa_tc.cu -- tcgen05 tensor-core kernel of the materialised-probability
-// SDPA forward (fp16 / bf16, head dim 64 or 128).
+// SDPA forward (fp16 / bf16, head dim 64 or 128, positive scale).
 //
 // What it computes: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- the
 // math backend's (out, attn_probs): P = softmax(scale*QK^T + mask), O = P V,
 // with a fully masked row giving P = O = 0.  P is normalised exactly through
 // the row log-sum-exp, the identity of the page's "P800 exact-P fast path"
-// update (P = exp(scale*QK^T - LSE)), which this kernel evaluates itself:
+// update (P = exp(scale*QK^T - LSE)), which the kernel evaluates in place:
 //
-//   sweep 1  S_j = Q K_j^T on the tensor cores (TMEM accumulator), running
-//            row max / sum of exp in the softmax warps -> lse per row;
-//   sweep 2  S_j again, p = exp2(S_j*scale*log2e - lse*log2e) written once
+//   sweep 1  S_j = Q K_j^T on the tensor cores (TMEM accumulator); running
+//            row max / sum of exp2 in the softmax warps -> lse per row;
+//   sweep 2  S_j again; p = exp2(S_j*scale*log2e - lse*log2e) written once
 //            as dtype into a 128B-swizzled shared tile that is both the A
 //            operand of O += P_j V_j (tensor cores) and the source of the TMA
-//            store of P; key tiles above a causal diagonal are never computed,
-//            their P region is written with zeros by TMA stores.
+//            stores of P.  Key tiles above a causal diagonal are never
+//            computed; their P region is written with zeros.
 //
-// One CTA owns a 128-row query tile of one (batch, head); 8 warps:
-//   warp 0      TMA producer (Q once; K tiles; then K/V tiles interleaved)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer
-//   warp 2      TMA store issuer for P tiles (and the zero tiles)
-//   warps 4..7  softmax / epilogue, one query row per thread (TMEM lane)
-// TMEM: S double buffer (2 x 128 columns) + O (D columns) in one 512-column
-// allocation.  Every mbarrier wait is bounded: a wait that runs out records
-// itself in the device status word and the CTA unwinds without hanging.
+// One CTA owns a 128-row query tile of one (batch, head); 12 warps:
+//   warp 0       TMA producer (Q once; K tiles; then K/V tiles interleaved)
+//   warp 1       TMEM allocator + single-thread tcgen05.mma issuer
+//   warps 2, 3   zero-fill of the P tiles above the causal diagonal
+//   warps 4..7   softmax warpgroup 0 (score tiles in S buffer 0 / P buffer 0)
+//   warps 8..11  softmax warpgroup 1 (score tiles in S buffer 1 / P buffer 1)
+// Score tiles alternate between the two buffers (tile counter mod 2 over both
+// sweeps).  Each softmax thread owns one query row (its TMEM lane); the groups
+// merge their sweep-1 row statistics through shared memory.  Each softmax
+// warp stores its own 32 rows of every P tile with TMA as soon as it has
+// written them.  After set-up the producer / MMA warpgroup hands registers to
+// the softmax warpgroups.  TMEM: two 128-column S buffers + O (D columns).
+//
+// Every mbarrier wait is bounded: a wait that runs out records itself in the
+// device status word and the CTA unwinds (freeing TMEM) instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -31,6 +38,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -47,6 +55,12 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr long long kWaitLimitCycles = 2000000000ll;  // ~1 s at GB300 clocks
+constexpr int kThreads = 384;
+// Register split after set-up: warpgroup 0 (producer / MMA / zero-fill warps)
+// gives registers up, the two softmax warpgroups take them.  The launch must
+// provide at least 128*kRegsLow + 256*kRegsHigh registers per CTA (checked on
+// the host before the first launch; setmaxnreg.inc would otherwise wait forever).
+constexpr uint32_t kRegsLow = 72, kRegsHigh = 200;
 
 // The three outer tensor-map dimensions are stored in stride order; a packed
 // code (2 bits per slot) says which logical dimension (1 = rows, 2 = head,
@@ -57,42 +71,16 @@ __device__ __forceinline__ int pick(uint32_t sel, int rows, int head, int batch)
 
 struct TcParams {
     int Sq, Skv, Hq, group, n_qtiles, causal;
-    float c2;  // scale * log2(e)
+    float c2;  // scale * log2(e), > 0
     const void* mask;
     int mask_kind, mask_dtype;
     long long sm0, sm1, sm2;
     void* o;
     long long so0, so1, so2;
     float* lse;
+    void* p;  // P (the zero tiles above a causal diagonal are written with plain stores)
+    long long sp0, sp1, sp2;
     uint32_t ord_q, ord_k, ord_v, ord_p;
-};
-
-template <int D>
-struct TcCfg {
-    static constexpr int kChunks = D / 64;               // 128-byte (64-element) column chunks
-    static constexpr int kTileBytes = 128 * D * 2;        // one Q / K / V tile
-    static constexpr int kStages = (D == 64) ? 6 : 3;     // K/V ring depth
-    static constexpr int kPBytes = 128 * 128 * 2;         // one P tile (2 chunks)
-    static constexpr int kZeroBytes = 128 * 64 * 2;       // one zero chunk
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kTileBytes;
-    static constexpr int kOffP = kOffKV + kStages * kTileBytes;
-    static constexpr int kOffZ = kOffP + 2 * kPBytes;
-    static constexpr int kOffBar = kOffZ + kZeroBytes;
-    // barrier indices
-    static constexpr int bQ = 0;
-    static constexpr int bKVF = 1;
-    static constexpr int bKVE = bKVF + kStages;
-    static constexpr int bSF = bKVE + kStages;
-    static constexpr int bSE = bSF + 2;
-    static constexpr int bPF = bSE + 2;
-    static constexpr int bPV = bPF + 2;
-    static constexpr int bPS = bPV + 2;
-    static constexpr int bO = bPS + 2;
-    static constexpr int kBars = bO + 1;
-    static constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
-    static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kTmemO = 256;
 };
 
 // Bounded mbarrier wait.  Returns false (after recording the first failure
@@ -132,8 +120,8 @@ template <> struct Pack<__nv_bfloat16> {
     }
 };
 
-// Mask value of (row, key) in base-2 units to add to the score: 0, -inf, or
-// an additive term.  Only called for rows < Sq and keys < Skv.
+// Base-2 additive term of a user mask at (row, key): 0 / -inf for a bool
+// mask, mask*log2(e) for an additive one.  Row and key must be in range.
 template <typename T>
 __device__ __forceinline__ float mask_term(const TcParams& p, int b, int h, int row, int key) {
     const long long off = b * p.sm0 + h * p.sm1 + row * p.sm2 + key;
@@ -145,8 +133,153 @@ __device__ __forceinline__ float mask_term(const TcParams& p, int b, int h, int 
     return m * kLog2e;
 }
 
-template <int D, typename T>
-__global__ void __launch_bounds__(256, 1)
+// ---------------------------------------------------------------- softmax tile helpers
+// s[] holds one row of a 128-key score tile.  Without a user mask it holds the
+// raw Q.K dot products (the base-2 scale is applied inside the exp2 FFMA,
+// cexp = scale*log2e); with a user mask it is scaled and masked first
+// (cexp = 1).  Masked entries are -inf either way.
+
+template <typename T, bool kMasked>
+__device__ __forceinline__ void mask_tile(float (&s)[128], const TcParams& prm, int b, int h, int row,
+                                          bool row_ok, int kv0) {
+    if constexpr (kMasked) {
+#pragma unroll
+        for (int x = 0; x < 128; ++x) {
+            const int key = kv0 + x;
+            const float add = (row_ok && key < prm.Skv) ? mask_term<T>(prm, b, h, row, key) : -CUDART_INF_F;
+            s[x] = fmaf(s[x], prm.c2, add);
+        }
+    }
+    int lim = prm.Skv - 1 - kv0;  // last visible key offset in this tile
+    if (prm.causal) lim = min(lim, row - kv0);
+    if (!row_ok) lim = -1;
+    if (lim < 127) {
+#pragma unroll
+        for (int x = 0; x < 128; ++x) s[x] = (x > lim) ? -CUDART_INF_F : s[x];
+    }
+}
+
+// Fold one tile into the running base-2 (max, sum of exp2) of the row.
+__device__ __forceinline__ void tile_stats(const float (&s)[128], float cexp, float& m, float& l) {
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+    for (int x = 8; x < 128; ++x) mx[x & 7] = fmaxf(mx[x & 7], s[x]);
+    const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                           fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cexp;
+    const float mn = fmaxf(m, mt);
+    if (mn != -CUDART_INF_F) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+        for (int x = 0; x < 128; ++x) acc[x & 7] += ex2(fmaf(s[x], cexp, -mn));
+        l = l * ex2(m - mn) + (((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7])));
+        m = mn;
+    }
+}
+
+// p = exp2(s*cexp - lse2), packed to dtype pairs.  neg_lse is -lse2, or -inf
+// for a fully masked row (every p becomes 0).
+template <typename T>
+__device__ __forceinline__ void tile_probs(const float (&s)[128], float cexp, float neg_lse, uint32_t (&hp)[64]) {
+#pragma unroll
+    for (int k = 0; k < 64; ++k)
+        hp[k] = Pack<T>::two(ex2(fmaf(s[2 * k], cexp, neg_lse)), ex2(fmaf(s[2 * k + 1], cexp, neg_lse)));
+}
+
+// One row of a P tile into the 128B-swizzled shared layout (two 64-key chunks
+// of 16 KB; 16-byte unit u of row t sits at unit u ^ (t % 8)).
+__device__ __forceinline__ void store_p_row(const uint32_t (&hp)[64], uint32_t tile_base, int t) {
+    const uint32_t rowaddr = tile_base + t * 128;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const uint32_t addr = rowaddr + (u / 8) * 16384 + (((u % 8) ^ (t % 8)) * 16);
+        st_shared_v4(addr, hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
+    }
+}
+
+// NCOL output columns of this thread's row from TMEM to global (16-byte stores).
+template <typename T, int NCOL>
+__device__ __forceinline__ void store_o_cols(uint32_t taddr, T* dst, bool row_ok, bool dead) {
+#pragma unroll
+    for (int c = 0; c < NCOL / 32; ++c) {
+        float ov[32];
+        tmem_ld32(taddr + c * 32, ov);
+        if (row_ok) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                uint4 pk;
+                pk.x = Pack<T>::two(dead ? 0.f : ov[u * 8 + 0], dead ? 0.f : ov[u * 8 + 1]);
+                pk.y = Pack<T>::two(dead ? 0.f : ov[u * 8 + 2], dead ? 0.f : ov[u * 8 + 3]);
+                pk.z = Pack<T>::two(dead ? 0.f : ov[u * 8 + 4], dead ? 0.f : ov[u * 8 + 5]);
+                pk.w = Pack<T>::two(dead ? 0.f : ov[u * 8 + 6], dead ? 0.f : ov[u * 8 + 7]);
+                *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = pk;
+            }
+        }
+    }
+}
+
+// Per-warp P store: once a warp has written its 32 rows of a P tile into
+// shared memory, its lane 0 stores them with two TMA boxes (64 keys x 32 rows
+// each).  Before the warp rewrites that buffer, lane 0 waits until the bulk
+// store has finished reading it.
+__device__ __forceinline__ void warp_store_p(const CUtensorMap* tm, uint32_t ord, uint32_t tile_base, int w,
+                                             int kv0, int r0, int h, int b) {
+    const int row = r0 + 32 * w;
+    for (int c = 0; c < 2; ++c)
+        tma_store_4d(tm, tile_base + c * 16384 + w * 32 * 128, kv0 + 64 * c, pick(ord & 3, row, h, b),
+                     pick((ord >> 2) & 3, row, h, b), pick((ord >> 4) & 3, row, h, b));
+    bulk_commit();
+}
+
+// Zero P[b, h, r0:r_end, z0:Skv] (the key tiles above a causal diagonal) with
+// 16-byte stores: warp `w` of `nwarps` takes every nwarps-th row and its lanes
+// cover consecutive 16-byte units of that row.  z0 is a multiple of 128 and
+// rows are 16-byte aligned.
+__device__ __forceinline__ void zero_p_region(const TcParams& prm, int b, int h, int r0, int r_end, int z0, int w,
+                                              int nwarps, int lane) {
+    if (z0 >= prm.Skv) return;
+    const int n = prm.Skv - z0, nvec = n / 8;
+    uint16_t* base = static_cast<uint16_t*>(prm.p) + b * prm.sp0 + h * prm.sp1 + z0;
+    for (int r = r0 + w; r < r_end; r += nwarps) {
+        uint16_t* row = base + (long long)r * prm.sp2;
+        for (int k = lane; k < nvec; k += 32) *reinterpret_cast<uint4*>(row + 8 * k) = make_uint4(0u, 0u, 0u, 0u);
+        if (lane < n - 8 * nvec) row[8 * nvec + lane] = 0;
+    }
+}
+
+__device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <int D>
+struct TcCfg {
+    static constexpr int kChunks = D / 64;               // 128-byte (64-element) column chunks
+    static constexpr int kTileBytes = 128 * D * 2;        // one Q / K / V tile
+    static constexpr int kStages = (D == 64) ? 8 : 4;     // K/V ring depth
+    static constexpr int kPBytes = 128 * 128 * 2;         // one P tile (2 chunks)
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffKV = kOffQ + kTileBytes;
+    static constexpr int kOffP = kOffKV + kStages * kTileBytes;
+    static constexpr int kOffStats = kOffP + 2 * kPBytes;  // float[2][128]: group 1's (m, l), then the lse
+    static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
+    // barrier indices
+    static constexpr int bQ = 0;
+    static constexpr int bKVF = 1;
+    static constexpr int bKVE = bKVF + kStages;
+    static constexpr int bSF = bKVE + kStages;   // [2] S buffer full  (MMA commit)
+    static constexpr int bSE = bSF + 2;          // [2] S buffer empty (128 softmax threads)
+    static constexpr int bPF = bSE + 2;          // [2] P buffer full  (128 softmax threads)
+    static constexpr int bPV = bPF + 2;          // [2] P buffer consumed by P V (MMA commit)
+    static constexpr int bO = bPV + 2;           // O complete (MMA commit)
+    static constexpr int kBars = bO + 1;
+    static constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
+    static constexpr uint32_t kTmemCols = 512;
+    static constexpr uint32_t kTmemO = 256;
+};
+
+template <int D, typename T, bool kMasked>
+__global__ void __launch_bounds__(kThreads, 1)
 tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_p,
                   const TcParams prm) {
@@ -158,7 +291,7 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sKV = smem_u32(smem + C::kOffKV);
     const uint32_t sP = smem_u32(smem + C::kOffP);
-    const uint32_t sZ = smem_u32(smem + C::kOffZ);
+    float* stat = reinterpret_cast<float*>(smem + C::kOffStats);  // [2][128]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -175,24 +308,14 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::bQ), 1);
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(bar(C::bKVF + s), 1);
-            mbar_init(bar(C::bKVE + s), 1);
-        }
+        for (int i = 0; i < C::kBars; ++i) mbar_init(bar(i), 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(C::bSF + i), 1);
             mbar_init(bar(C::bSE + i), 128);
             mbar_init(bar(C::bPF + i), 128);
-            mbar_init(bar(C::bPV + i), 1);
-            mbar_init(bar(C::bPS + i), 1);
         }
-        mbar_init(bar(C::bO), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < C::kZeroBytes / 16; i += blockDim.x) st_shared_v4(sZ + i * 16, 0, 0, 0, 0);
-    fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
@@ -202,210 +325,168 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------------------ TMA producer
-        prefetch_tmap(&tm_q);
-        prefetch_tmap(&tm_k);
-        prefetch_tmap(&tm_v);
-        mbar_arrive_expect_tx(bar(C::bQ), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sQ + c * 16384, &tm_q, bar(C::bQ), c * 64, pick(prm.ord_q & 3, r0, h, b),
-                        pick((prm.ord_q >> 2) & 3, r0, h, b), pick((prm.ord_q >> 4) & 3, r0, h, b));
-        int it = 0;
-        auto load = [&](const CUtensorMap* tm, uint32_t ord, int kv0) {
-            const int s = it % C::kStages;
-            const uint32_t ph = (it / C::kStages) & 1;
-            wait_bar(bar(C::bKVE + s), ph ^ 1, abort_flag, 1, C::bKVE + s);
-            mbar_arrive_expect_tx(bar(C::bKVF + s), C::kTileBytes);
+    if (warp < 4) {  // producer / MMA / zero-fill warpgroup
+        setmaxnreg_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(bar(C::bQ), C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sKV + s * C::kTileBytes + c * 16384, tm, bar(C::bKVF + s), c * 64,
-                            pick(ord & 3, kv0, hk, b), pick((ord >> 2) & 3, kv0, hk, b),
-                            pick((ord >> 4) & 3, kv0, hk, b));
-            ++it;
-        };
-        for (int j = 0; j < n_live; ++j) load(&tm_k, prm.ord_k, j * 128);
-        load(&tm_k, prm.ord_k, 0);
-        for (int j = 1; j < n_live; ++j) {
-            load(&tm_k, prm.ord_k, j * 128);
-            load(&tm_v, prm.ord_v, (j - 1) * 128);
-        }
-        load(&tm_v, prm.ord_v, (n_live - 1) * 128);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
-        constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
-        wait_bar(bar(C::bQ), 0, abort_flag, 2, C::bQ);
-        int it = 0, sc = 0;
-        auto qk = [&]() {
-            const int s = it % C::kStages;
-            wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
-            const int buf = sc & 1;
-            wait_bar(bar(C::bSE + buf), ((sc >> 1) & 1) ^ 1, abort_flag, 2, C::bSE + buf);
-            tc_fence_after();
-            const uint32_t d = tmem + buf * 128;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                tc_mma_f16(d, sw128_desc(sQ + off, 16, 1024), sw128_desc(sKV + s * C::kTileBytes + off, 16, 1024),
-                           idesc_qk, kk > 0 ? 1u : 0u);
+                tma_load_4d(sQ + c * 16384, &tm_q, bar(C::bQ), c * 64, pick(prm.ord_q & 3, r0, h, b),
+                            pick((prm.ord_q >> 2) & 3, r0, h, b), pick((prm.ord_q >> 4) & 3, r0, h, b));
+            int it = 0;
+            auto load = [&](const CUtensorMap* tm, uint32_t ord, int kv0) {
+                const int s = it % C::kStages;
+                const uint32_t ph = (it / C::kStages) & 1;
+                wait_bar(bar(C::bKVE + s), ph ^ 1, abort_flag, 1, C::bKVE + s);
+                mbar_arrive_expect_tx(bar(C::bKVF + s), C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sKV + s * C::kTileBytes + c * 16384, tm, bar(C::bKVF + s), c * 64,
+                                pick(ord & 3, kv0, hk, b), pick((ord >> 2) & 3, kv0, hk, b),
+                                pick((ord >> 4) & 3, kv0, hk, b));
+                ++it;
+            };
+            // the MMA issuer consumes: K_0..K_{n-1} (sweep 1); then K_0, K_1 and,
+            // for each j, K_{j+2} (when it exists) followed by V_j (sweep 2)
+            for (int j = 0; j < n_live; ++j) load(&tm_k, prm.ord_k, j * 128);
+            for (int j = 0; j < min(2, n_live); ++j) load(&tm_k, prm.ord_k, j * 128);
+            for (int j = 0; j < n_live; ++j) {
+                if (j + 2 < n_live) load(&tm_k, prm.ord_k, (j + 2) * 128);
+                load(&tm_v, prm.ord_v, j * 128);
             }
-            tc_commit(bar(C::bKVE + s));
-            tc_commit(bar(C::bSF + buf));
-            ++it;
-            ++sc;
-        };
-        auto pv = [&](int j) {
-            const int pb = j & 1;
-            wait_bar(bar(C::bPF + pb), (j >> 1) & 1, abort_flag, 2, C::bPF + pb);
-            const int s = it % C::kStages;
-            wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
-            tc_fence_after();
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
+            wait_bar(bar(C::bQ), 0, abort_flag, 2, C::bQ);
+            int it = 0, sc = 0;
+            int pv_use0 = 0, pv_use1 = 0;
+            auto qk = [&]() {
+                const int s = it % C::kStages;
+                wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
+                const int buf = sc & 1;
+                wait_bar(bar(C::bSE + buf), ((sc >> 1) & 1) ^ 1, abort_flag, 2, C::bSE + buf);
+                tc_fence_after();
+                const uint32_t d = tmem + buf * 128;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;  // P: K-major, 16 keys per step
-                const uint32_t b_off = kk * 2048;                         // V: N-major, 16 key rows per step
-                tc_mma_f16(tmem + C::kTmemO, sw128_desc(sP + pb * C::kPBytes + a_off, 16, 1024),
-                           sw128_desc(sKV + s * C::kTileBytes + b_off, 16384, 1024), idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    tc_mma_f16(d, sw128_desc(sQ + off, 16, 1024),
+                               sw128_desc(sKV + s * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(C::bKVE + s));
+                tc_commit(bar(C::bSF + buf));
+                ++it;
+                ++sc;
+            };
+            auto pv = [&](int j) {
+                const int pb = (n_live + j) & 1;  // sweep-2 tile j lives in S / P buffer (n + j) mod 2
+                const int use = pb ? pv_use1++ : pv_use0++;
+                wait_bar(bar(C::bPF + pb), use & 1, abort_flag, 2, C::bPF + pb);
+                const int s = it % C::kStages;
+                wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;  // P: K-major, 16 keys per step
+                    const uint32_t b_off = kk * 2048;                         // V: N-major, 16 key rows per step
+                    tc_mma_f16(tmem + C::kTmemO, sw128_desc(sP + pb * C::kPBytes + a_off, 16, 1024),
+                               sw128_desc(sKV + s * C::kTileBytes + b_off, 16384, 1024), idesc_pv,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(C::bKVE + s));
+                tc_commit(bar(C::bPV + pb));
+                ++it;
+            };
+            // sweep 1, then sweep 2 with S two tiles ahead of P V, so that the
+            // scores a softmax group needs next never wait behind the other
+            // group's P tile
+            for (int j = 0; j < n_live; ++j) qk();
+            for (int j = 0; j < min(2, n_live); ++j) qk();
+            for (int j = 0; j < n_live; ++j) {
+                if (j + 2 < n_live) qk();
+                pv(j);
             }
-            tc_commit(bar(C::bKVE + s));
-            tc_commit(bar(C::bPV + pb));
-            ++it;
-        };
-        for (int j = 0; j < n_live; ++j) qk();
-        qk();
-        for (int j = 1; j < n_live; ++j) {
-            qk();
-            pv(j - 1);
+            tc_commit(bar(C::bO));
+        } else if (warp >= 2) {
+            // ------------------------------------------------------------ causal zero tiles
+            zero_p_region(prm, b, h, r0, r_last + 1, n_live * 128, warp - 2, 2, lane);
         }
-        pv(n_live - 1);
-        tc_commit(bar(C::bO));
-    } else if (warp == 2 && lane == 0) {
-        // ------------------------------------------------------------ P store issuer
-        prefetch_tmap(&tm_p);
-        const uint32_t o = prm.ord_p;
-        for (int jz = n_live; jz < n_all; ++jz)
-            for (int c = 0; c < 2; ++c)
-                tma_store_4d(&tm_p, sZ, jz * 128 + c * 64, pick(o & 3, r0, h, b), pick((o >> 2) & 3, r0, h, b),
-                             pick((o >> 4) & 3, r0, h, b));
-        bulk_commit();
-        for (int j = 0; j < n_live; ++j) {
-            const int pb = j & 1;
-            wait_bar(bar(C::bPF + pb), (j >> 1) & 1, abort_flag, 3, C::bPF + pb);
-            for (int c = 0; c < 2; ++c)
-                tma_store_4d(&tm_p, sP + pb * C::kPBytes + c * 16384, j * 128 + c * 64, pick(o & 3, r0, h, b),
-                             pick((o >> 2) & 3, r0, h, b), pick((o >> 4) & 3, r0, h, b));
-            bulk_commit();
-            bulk_wait_read0();
-            mbar_arrive(bar(C::bPS + pb));
-        }
-        bulk_wait0();
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ softmax + epilogue
-        const int t = threadIdx.x - 128;  // row within the tile == TMEM lane
+    } else {
+        // ------------------------------------------------------------ softmax warpgroups
+        setmaxnreg_inc<kRegsHigh>();
+        const int wg = (warp - 4) >> 2;           // owns S buffer wg and P buffer wg
+        const int t = (threadIdx.x - 128) & 127;  // row within the tile == TMEM lane
         const int row = r0 + t;
         const bool row_ok = row < prm.Sq;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const float c2 = prm.c2;
-        const bool has_mask = prm.mask_kind != kMaskNone;
+        const uint32_t s_tmem = tmem + lane_base + wg * 128;
+        const float cexp = kMasked ? 1.f : prm.c2;
         float s[128];
-        int sc = 0;
 
-        auto load_s = [&](int role) {
-            const int buf = sc & 1;
-            wait_bar(bar(C::bSF + buf), (sc >> 1) & 1, abort_flag, role, C::bSF + buf);
+        auto load_s = [&](int sc, int role) {
+            wait_bar(bar(C::bSF + wg), (sc >> 1) & 1, abort_flag, role, C::bSF + wg);
             tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_base + buf * 128 + c * 32, s + c * 32);
+            tmem_ld128(s_tmem, s);
             tc_fence_before();
-            mbar_arrive(bar(C::bSE + buf));
-            ++sc;
-        };
-        // scale to base 2 and apply causal / ragged / user masking in place
-        auto scale_mask = [&](int kv0) {
-            const bool edge = (prm.causal && kv0 + 127 > r0) || (kv0 + 128 > prm.Skv) || !row_ok;
-#pragma unroll
-            for (int x = 0; x < 128; ++x) s[x] *= c2;
-            if (edge || has_mask) {
-#pragma unroll
-                for (int x = 0; x < 128; ++x) {
-                    const int key = kv0 + x;
-                    float add = 0.f;
-                    if (!row_ok || key >= prm.Skv || (prm.causal && key > row)) add = -CUDART_INF_F;
-                    else if (has_mask) add = mask_term<T>(prm, b, h, row, key);
-                    s[x] += add;
-                }
-            }
+            mbar_arrive(bar(C::bSE + wg));
         };
 
-        // sweep 1: row max and sum of exp2
+        // sweep 1: this group's score tiles -> partial row max / sum of exp2
         float m = -CUDART_INF_F, l = 0.f;
-        for (int j = 0; j < n_live; ++j) {
-            load_s(4);
-            scale_mask(j * 128);
-            float mt = -CUDART_INF_F;
-#pragma unroll
-            for (int x = 0; x < 128; ++x) mt = fmaxf(mt, s[x]);
-            const float mn = fmaxf(m, mt);
-            if (mn != -CUDART_INF_F) {
-                float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll
-                for (int x = 0; x < 128; x += 4) {
-                    acc0 += ex2(s[x] - mn);
-                    acc1 += ex2(s[x + 1] - mn);
-                    acc2 += ex2(s[x + 2] - mn);
-                    acc3 += ex2(s[x + 3] - mn);
-                }
-                l = l * ex2(m - mn) + ((acc0 + acc1) + (acc2 + acc3));
-                m = mn;
-            }
+        for (int sc = wg; sc < n_live; sc += 2) {
+            load_s(sc, 4);
+            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, sc * 128);
+            tile_stats(s, cexp, m, l);
         }
-        const float lse2 = (m == -CUDART_INF_F) ? -CUDART_INF_F : m + log2f(l);
+        // merge the two groups' statistics: group 1 publishes (m, l), group 0
+        // forms the row lse and publishes it, group 1 reads it back (both groups
+        // then hold bit-identical values)
+        if (wg == 1) {
+            stat[t] = m;
+            stat[128 + t] = l;
+        }
+        softmax_group_sync();
+        if (wg == 0) {
+            const float m1 = stat[t], l1 = stat[128 + t];
+            const float mm = fmaxf(m, m1);
+            stat[t] = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(l * ex2(m - mm) + l1 * ex2(m1 - mm));
+        }
+        softmax_group_sync();
+        const float lse2 = stat[t];
         const bool dead = lse2 == -CUDART_INF_F;
+        const float neg_lse = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
+        if (lane == 0) prefetch_tmap(&tm_p);
 
-        // sweep 2: exact P into the swizzled shared tile
-        for (int j = 0; j < n_live; ++j) {
-            load_s(5);
-            scale_mask(j * 128);
-            const int pb = j & 1;
-            const uint32_t ph = ((j >> 1) & 1) ^ 1;
-            wait_bar(bar(C::bPV + pb), ph, abort_flag, 5, C::bPV + pb);
-            wait_bar(bar(C::bPS + pb), ph, abort_flag, 5, C::bPS + pb);
-            const uint32_t rowaddr = sP + pb * C::kPBytes + t * 128;
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) p[e] = dead ? 0.f : ex2(s[u * 8 + e] - lse2);
-                const uint32_t addr = rowaddr + (u / 8) * 16384 + (((u % 8) ^ (t % 8)) * 16);
-                st_shared_v4(addr, Pack<T>::two(p[0], p[1]), Pack<T>::two(p[2], p[3]), Pack<T>::two(p[4], p[5]),
-                             Pack<T>::two(p[6], p[7]));
-            }
+        // sweep 2: exact P into this group's swizzled shared tile, then TMA stores
+        int use = 0;
+        for (int sc = n_live + ((wg - n_live) & 1); sc < 2 * n_live; sc += 2) {
+            const int j = sc - n_live;
+            load_s(sc, 5);
+            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+            uint32_t hp[64];
+            tile_probs<T>(s, cexp, neg_lse, hp);
+            wait_bar(bar(C::bPV + wg), (use & 1) ^ 1, abort_flag, 5, C::bPV + wg);
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            store_p_row(hp, sP + wg * C::kPBytes, t);
             fence_proxy_async_smem();
-            mbar_arrive(bar(C::bPF + pb));
+            mbar_arrive(bar(C::bPF + wg));
+            __syncwarp();
+            if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + wg * C::kPBytes, warp & 3, j * 128, r0, h, b);
+            ++use;
         }
+        if (lane == 0) bulk_wait0();
 
-        // epilogue: O from TMEM, direct 16-byte stores of this thread's row
+        // epilogue: this group's half of the O columns
         wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
         tc_fence_after();
         T* orow = static_cast<T*>(prm.o) + b * prm.so0 + h * prm.so1 + (long long)row * prm.so2;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-            float ov[32];
-            tmem_ld32(tmem + lane_base + C::kTmemO + c * 32, ov);
-            if (row_ok) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    uint4 pk;
-                    pk.x = Pack<T>::two(dead ? 0.f : ov[u * 8 + 0], dead ? 0.f : ov[u * 8 + 1]);
-                    pk.y = Pack<T>::two(dead ? 0.f : ov[u * 8 + 2], dead ? 0.f : ov[u * 8 + 3]);
-                    pk.z = Pack<T>::two(dead ? 0.f : ov[u * 8 + 4], dead ? 0.f : ov[u * 8 + 5]);
-                    pk.w = Pack<T>::two(dead ? 0.f : ov[u * 8 + 6], dead ? 0.f : ov[u * 8 + 7]);
-                    *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = pk;
-                }
-            }
-        }
-        if (prm.lse && row_ok) prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
+        store_o_cols<T, D / 2>(tmem + lane_base + C::kTmemO + wg * (D / 2), orow + wg * (D / 2), row_ok, dead);
+        if (wg == 0 && prm.lse && row_ok)
+            prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
     }
 
     // ------------------------------------------------------------ teardown
@@ -437,10 +518,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D tensor map over a logical [B, H, S, X] tensor (X contiguous) with a box
-// of 64 x 128 rows, 128-byte swizzle.  The three outer dims are ordered by
+// of 64 x box_rows rows, 128-byte swizzle.  The three outer dims are ordered by
 // stride; `ord` receives the packed order code.
-bool make_map(CUtensorMap* map, int dtype, const void* base, long long X, long long S, long long H, long long Bn,
-              const int64_t* st /* [B, H, S] element strides */, uint32_t* ord) {
+bool encode_map(CUtensorMap* map, int dtype, const void* base, long long X, long long S, long long H, long long Bn,
+                const int64_t* st /* [B, H, S] element strides */, uint32_t box_rows, uint32_t* ord) {
     auto fn = encode_fn();
     if (!fn) return false;
     struct Dim { long long ext, stride; int sel; };
@@ -458,7 +539,7 @@ bool make_map(CUtensorMap* map, int dtype, const void* base, long long X, long l
         dims[k + 1] = (cuuint64_t)d[k].ext;
         strides[k] = (cuuint64_t)(d[k].stride * 2);
         if (strides[k] % 16 != 0) return false;
-        box[k + 1] = d[k].sel == 1 ? 128 : 1;
+        box[k + 1] = d[k].sel == 1 ? box_rows : 1;
         code |= (uint32_t)d[k].sel << (2 * k);
     }
     cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -469,6 +550,49 @@ bool make_map(CUtensorMap* map, int dtype, const void* base, long long X, long l
     return r == CUDA_SUCCESS;
 }
 
+// Small cache of encoded tensor maps, so that repeated calls on the same
+// buffers skip the host-side encode.  Keyed by everything the encode reads.
+struct MapKey {
+    const void* base;
+    long long X, S, H, Bn, s0, s1, s2;
+    int dtype;
+    uint32_t box_rows;
+    bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    uint32_t ord;
+    bool used;
+};
+constexpr int kMapCache = 64;
+std::mutex g_map_mu;
+MapEntry g_maps[kMapCache];
+int g_map_next = 0;
+
+bool make_map(CUtensorMap* map, int dtype, const void* base, long long X, long long S, long long H, long long Bn,
+              const int64_t* st, uint32_t box_rows, uint32_t* ord) {
+    MapKey key;
+    std::memset(&key, 0, sizeof(key));
+    key.base = base; key.X = X; key.S = S; key.H = H; key.Bn = Bn;
+    key.s0 = st[0]; key.s1 = st[1]; key.s2 = st[2]; key.dtype = dtype; key.box_rows = box_rows;
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (auto& e : g_maps)
+        if (e.used && e.key == key) {
+            *map = e.map;
+            *ord = e.ord;
+            return true;
+        }
+    if (!encode_map(map, dtype, base, X, S, H, Bn, st, box_rows, ord)) return false;
+    MapEntry& e = g_maps[g_map_next];
+    g_map_next = (g_map_next + 1) % kMapCache;
+    e.key = key;
+    e.map = *map;
+    e.ord = *ord;
+    e.used = true;
+    return true;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool strides_ok(const int64_t* st, const int64_t* ext) {
@@ -477,16 +601,52 @@ bool strides_ok(const int64_t* st, const int64_t* ext) {
     return true;
 }
 
-template <int D, typename T>
+// One-time (per kernel instantiation and device) launch preparation: the
+// register check of the in-kernel split and the shared-memory opt-in.  Keyed
+// by the kernel's address (every instantiation has the same pointer type).
+struct Prepared {
+    const void* kern;
+    int dev;
+    int state;  // 1 = ready, 2 = refused
+};
+std::mutex g_prep_mu;
+Prepared g_prep[64];
+int g_prep_n = 0;
+
+template <typename K>
+cudaError_t prepare_kernel(K kern, int smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const void* key = reinterpret_cast<const void*>(kern);
+    std::lock_guard<std::mutex> lock(g_prep_mu);
+    for (int i = 0; i < g_prep_n; ++i)
+        if (g_prep[i].kern == key && g_prep[i].dev == dev)
+            return g_prep[i].state == 1 ? cudaSuccess : cudaErrorNotSupported;
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    int state = 1;
+    // the in-kernel register split must fit what the launch allocates
+    if (fa.numRegs * kThreads < (int)(128 * kRegsLow + 256 * kRegsHigh)) state = 2;
+    if (state == 1) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    if (g_prep_n < 64) g_prep[g_prep_n++] = Prepared{key, dev, state};
+    return state == 1 ? cudaSuccess : cudaErrorNotSupported;
+}
+
+template <int D, typename T, bool kMasked>
 cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
     using C = TcCfg<D>;
     CUtensorMap mq, mk, mv, mp;
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
-    if (!make_map(&mq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, &prm.ord_q) ||
-        !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, &prm.ord_k) ||
-        !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, &prm.ord_v) ||
-        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, &prm.ord_p))
+    if (!make_map(&mq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, 128, &prm.ord_q) ||
+        !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, 128, &prm.ord_k) ||
+        !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 128, &prm.ord_v) ||
+        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 32, &prm.ord_p))
         return cudaErrorNotSupported;
     prm.Sq = (int)p.Sq;
     prm.Skv = (int)p.Skv;
@@ -502,12 +662,21 @@ cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
     prm.o = p.o;
     prm.so0 = p.so[0]; prm.so1 = p.so[1]; prm.so2 = p.so[2];
     prm.lse = p.lse;
-    auto kern = tc_twopass_kernel<D, T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    prm.p = p.p;
+    prm.sp0 = p.sp[0]; prm.sp1 = p.sp[1]; prm.sp2 = p.sp[2];
+    auto kern = tc_twopass_kernel<D, T, kMasked>;
+    cudaError_t e = prepare_kernel(kern, C::kSmem);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)prm.n_qtiles);
-    kern<<<grid, 256, C::kSmem, stream>>>(mq, mk, mv, mp, prm);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(mq, mk, mv, mp, prm);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
+    const bool masked = p.mask_kind != kMaskNone;
+    if (p.D == 64) return masked ? launch_twopass<64, T, true>(p, stream) : launch_twopass<64, T, false>(p, stream);
+    return masked ? launch_twopass<128, T, true>(p, stream) : launch_twopass<128, T, false>(p, stream);
 }
 
 }  // namespace
@@ -517,6 +686,7 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
     if (p.dtype != kF16 && p.dtype != kBF16) { *why = "dtype must be f16 or bf16"; return false; }
     if (p.D != p.Dv || (p.D != 64 && p.D != 128)) { *why = "head dim must be 64 or 128 (D == Dv)"; return false; }
     if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
+    if (!(p.scale > 0.f)) { *why = "scale must be positive"; return false; }
     if (p.Sq >= (1ll << 31) || p.Skv >= (1ll << 31) || p.B > 65535 || p.Sq > 65535ll * 128) {
         *why = "sizes beyond the grid limits"; return false;
     }
@@ -534,9 +704,7 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
 cudaError_t launch_tc(const Problem& p, bool fused, cudaStream_t stream) {
     const char* why;
     if (!tc_supports(p, fused, &why)) return cudaErrorNotSupported;
-    if (p.dtype == kF16)
-        return p.D == 64 ? launch_twopass<64, __half>(p, stream) : launch_twopass<128, __half>(p, stream);
-    return p.D == 64 ? launch_twopass<64, __nv_bfloat16>(p, stream) : launch_twopass<128, __nv_bfloat16>(p, stream);
+    return p.dtype == kF16 ? launch_t<__half>(p, stream) : launch_t<__nv_bfloat16>(p, stream);
 }
 
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int* value) {
