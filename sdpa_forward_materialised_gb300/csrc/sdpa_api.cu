@@ -14,7 +14,7 @@
 #include <cstring>
 #include <string>
 
-#include "../../include/sdpa_math.h"
+#include "sdpa_math.h"  // include/ is on the compiler search path
 #include "internal.h"
 
 namespace {

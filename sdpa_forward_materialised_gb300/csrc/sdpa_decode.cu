@@ -1,13 +1,440 @@
-// sdpa_decode.cu -- split-KV decode kernel; placeholder until it lands.
+// sdpa_decode.cu -- materialised-probability SDPA forward for few query rows
+// per key/value head (decode: Hq/Hkv * Sq <= 16 rows), split over the keys
+// across a thread-block cluster.
+//
+// What it computes: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- the
+// math backend's (out, attn_probs) with P normalised exactly through the row
+// log-sum-exp (the page's "P800 exact-P fast path" identity
+// P = exp(scale*QK^T - LSE)); fully masked rows give P = O = 0.
+//
+// With a handful of query rows the work is bound by reading K and V once from
+// HBM, and a 128-row tensor-core tile would be mostly empty.  So one cluster
+// of C CTAs owns one (batch, key/value head) and all R = group * Sq query rows
+// that read it; CTA rank c owns a contiguous chunk of the keys:
+//   1. start asynchronous copies of the V chunk into shared memory; stage
+//      the R query rows as fp32;
+//   2. scores: one thread per key loads its K row straight into registers
+//      (16-byte loads, eight in flight) and forms the R dot products (FFMA,
+//      base-2 units, masking); per-row (max, sum of exp2) of the chunk;
+//   3. cluster barrier; every CTA reads the C partial statistics through
+//      distributed shared memory and forms the same lse per row;
+//   4. P for the chunk (coalesced stores) and the partial O = P_chunk V_chunk
+//      from the rounded P; cluster barrier;
+//   5. CTA c sums its slice of the O columns over the cluster (distributed
+//      shared memory) and stores O; a last cluster barrier keeps every CTA's
+//      shared memory alive until all reads are done.
+// No global workspace is used and every CTA reaches every cluster barrier.
+// A CTA needs little shared memory (the V chunk, the scores, the partial O),
+// so all clusters of a decode-sized call are resident at once and every K and
+// V read of the call is issued in the first few microseconds.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "internal.h"
 
 namespace sdpa {
+namespace {
 
-bool decode_supports(const Problem&, const char** why) {
-    *why = "decode kernel is not built yet";
-    return false;
+constexpr int kThreads = 256;
+constexpr int kMaxRows = 16;     // query rows per (batch, kv head)
+constexpr int kMaxCluster = 8;   // portable cluster size
+constexpr int kSmemBudget = 160 * 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__half>(__half x) { return __half2float(x); }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __half from_f<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// the two elements of a packed pair of 16-bit values
+template <typename T> __device__ __forceinline__ float2 unpack2(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+template <> __device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
 }
 
-cudaError_t launch_decode(const Problem&, cudaStream_t) { return cudaErrorNotSupported; }
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of the same shared-memory word in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
+    uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+struct DecParams {
+    const void* q; long long sq0, sq1, sq2;
+    const void* k; long long sk0, sk1, sk2;
+    const void* v; long long sv0, sv1, sv2;
+    const void* mask; int mask_kind, mask_dtype; long long sm0, sm1, sm2;
+    void* o; long long so0, so1, so2;
+    void* p; long long sp0, sp1, sp2;
+    float* lse;
+    int Hq, Sq, Skv, D, Dv, group, rows, chunk, causal;
+    float c2;  // scale * log2(e)
+    int off_v, off_q, off_s, off_o, off_stat;  // shared-memory layout (bytes)
+};
+
+// RM is a compile-time bound on the query rows (R <= RM), so the per-row
+// accumulators of the score phase stay in registers.
+template <typename T, int RM>
+__global__ void __launch_bounds__(kThreads, RM <= 8 ? 4 : 3)
+decode_kernel(const DecParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float lse_s[kMaxRows];
+    __shared__ int row_h[kMaxRows], row_i[kMaxRows];
+
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    const uint32_t crank = cluster_rank();
+    const int C = (int)(gridDim.x);  // the cluster spans the x dimension
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int k0 = (int)crank * p.chunk;
+    const int n = max(0, min(p.Skv, k0 + p.chunk) - k0);  // keys of this CTA (may be 0)
+    const int R = p.rows, D = p.D, Dv = p.Dv;
+
+    uint8_t* vs = smem + p.off_v;                             // [n][Dv] V chunk (dtype)
+    float* qs = reinterpret_cast<float*>(smem + p.off_q);     // [R][D] query rows (fp32)
+    float* ss = reinterpret_cast<float*>(smem + p.off_s);     // [R][chunk] scores, then rounded P
+    float* op = reinterpret_cast<float*>(smem + p.off_o);     // [R][Dv] partial O
+    float* st = reinterpret_cast<float*>(smem + p.off_stat);  // [R][2] chunk (max, sum)
+
+    // ---- 1. asynchronous copy of the V chunk; query rows as fp32
+    const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
+    const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
+    {
+        const int uv = Dv * (int)sizeof(T) / 16;  // 16-byte units per V row
+        for (int u = t; u < n * uv; u += kThreads) {
+            const int r = u / uv, c = u % uv;
+            cp_async16(vs + 16 * u, reinterpret_cast<const uint8_t*>(V + r * p.sv2) + 16 * c);
+        }
+        cp_async_commit();
+    }
+    if (t < R) {
+        row_h[t] = hk * p.group + t / p.Sq;
+        row_i[t] = t % p.Sq;
+    }
+    __syncthreads();
+    for (int e = t; e < R * D; e += kThreads) {
+        const int r = e / D, d = e % D;
+        const T* qr = static_cast<const T*>(p.q) + b * p.sq0 + row_h[r] * p.sq1 + (long long)row_i[r] * p.sq2;
+        qs[r * D + d] = to_f(qr[d]);
+    }
+    __syncthreads();
+
+    // ---- 2. scores: thread j owns key k0 + j and reads its K row straight
+    // into registers, 128 bytes (eight 16-byte loads in flight) per batch
+    if (t < n) {
+        const uint8_t* krow = reinterpret_cast<const uint8_t*>(K + (long long)t * p.sk2);
+        const int kbytes = D * (int)sizeof(T);
+        constexpr int kE = 16 / (int)sizeof(T);  // elements per 16-byte unit
+        float acc[RM];
+#pragma unroll
+        for (int r = 0; r < RM; ++r) acc[r] = 0.f;
+        for (int b0 = 0; b0 < kbytes; b0 += 128) {
+            uint4 kx[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (b0 + 16 * u < kbytes) kx[u] = __ldg(reinterpret_cast<const uint4*>(krow + b0 + 16 * u));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (b0 + 16 * u >= kbytes) break;
+                const int d = (b0 + 16 * u) / (int)sizeof(T);
+                if constexpr (sizeof(T) == 4) {
+                    const float4 kk = make_float4(__uint_as_float(kx[u].x), __uint_as_float(kx[u].y),
+                                                  __uint_as_float(kx[u].z), __uint_as_float(kx[u].w));
+#pragma unroll
+                    for (int r = 0; r < RM; ++r)
+                        if (r < R) {
+                            const float4 qq = *reinterpret_cast<const float4*>(&qs[r * D + d]);
+                            float a = acc[r];
+                            a = fmaf(qq.x, kk.x, a);
+                            a = fmaf(qq.y, kk.y, a);
+                            a = fmaf(qq.z, kk.z, a);
+                            a = fmaf(qq.w, kk.w, a);
+                            acc[r] = a;
+                        }
+                } else {
+                    static_assert(kE == 8, "16-bit elements");
+                    const float2 k01 = unpack2<T>(kx[u].x), k23 = unpack2<T>(kx[u].y);
+                    const float2 k45 = unpack2<T>(kx[u].z), k67 = unpack2<T>(kx[u].w);
+#pragma unroll
+                    for (int r = 0; r < RM; ++r)
+                        if (r < R) {
+                            const float4 qa = *reinterpret_cast<const float4*>(&qs[r * D + d]);
+                            const float4 qb = *reinterpret_cast<const float4*>(&qs[r * D + d + 4]);
+                            float a = acc[r];
+                            a = fmaf(qa.x, k01.x, a);
+                            a = fmaf(qa.y, k01.y, a);
+                            a = fmaf(qa.z, k23.x, a);
+                            a = fmaf(qa.w, k23.y, a);
+                            a = fmaf(qb.x, k45.x, a);
+                            a = fmaf(qb.y, k45.y, a);
+                            a = fmaf(qb.z, k67.x, a);
+                            a = fmaf(qb.w, k67.y, a);
+                            acc[r] = a;
+                        }
+                }
+            }
+        }
+        const int key = k0 + t;
+#pragma unroll
+        for (int r = 0; r < RM; ++r)
+            if (r < R) {
+                float s = __fmul_rn(acc[r], p.c2);
+                if (p.causal && key > row_i[r]) s = -CUDART_INF_F;
+                if (p.mask_kind != kMaskNone) {
+                    const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + key;
+                    if (p.mask_kind == kMaskBool) {
+                        if (static_cast<const unsigned char*>(p.mask)[off] == 0) s = -CUDART_INF_F;
+                    } else {
+                        const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                             : to_f(static_cast<const T*>(p.mask)[off]);
+                        s = __fmaf_rn(m, kLog2e, s);
+                    }
+                }
+                ss[r * p.chunk + t] = s;
+            }
+    }
+    __syncthreads();
+
+    // per-row (max, sum of exp2) of the chunk: one warp per row
+    for (int r = warp; r < R; r += kThreads / 32) {
+        float m = -CUDART_INF_F;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, ss[r * p.chunk + j]);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        if (m != -CUDART_INF_F)
+            for (int j = lane; j < n; j += 32) l += exp2f(ss[r * p.chunk + j] - m);
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            st[2 * r] = m;
+            st[2 * r + 1] = l;
+        }
+    }
+
+    // ---- 3. the cluster's statistics -> the same lse in every CTA
+    cluster_sync();
+    if (t < R) {
+        float mc[kMaxCluster], lc[kMaxCluster];  // all peer loads first, then the merge
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) {
+                mc[c] = ld_peer(peer_addr(&st[2 * t], (uint32_t)c));
+                lc[c] = ld_peer(peer_addr(&st[2 * t + 1], (uint32_t)c));
+            }
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) m = fmaxf(m, mc[c]);
+        float l = 0.f;
+        if (m != -CUDART_INF_F) {
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (c < C && mc[c] != -CUDART_INF_F) l += lc[c] * exp2f(mc[c] - m);
+        }
+        lse_s[t] = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
+    }
+    __syncthreads();
+
+    // ---- 4. P for the chunk (stored, then kept rounded for P V)
+    for (int e = t; e < R * n; e += kThreads) {
+        const int r = e / n, j = e % n;
+        const float L = lse_s[r];
+        const float pr = (L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L);
+        const T pt = from_f<T>(pr);
+        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
+        prow[k0 + j] = pt;
+        ss[r * p.chunk + j] = to_f(pt);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    // partial O = P_chunk V_chunk; a thread item is (row, pair of columns)
+    // (Dv is even: V rows are 16-byte multiples)
+    const int dv2 = Dv / 2;
+    for (int e = t; e < R * dv2; e += kThreads) {
+        const int r = e / dv2, d = 2 * (e % dv2);
+        const float* pr = ss + r * p.chunk;
+        float a0 = 0.f, a1 = 0.f;
+        for (int j = 0; j < n; ++j) {
+            float2 vv;
+            if constexpr (sizeof(T) == 4) vv = *reinterpret_cast<const float2*>(vs + (j * Dv + d) * 4);
+            else vv = unpack2<T>(*reinterpret_cast<const uint32_t*>(vs + (j * Dv + d) * 2));
+            a0 = fmaf(pr[j], vv.x, a0);
+            a1 = fmaf(pr[j], vv.y, a1);
+        }
+        *reinterpret_cast<float2*>(&op[r * Dv + d]) = make_float2(a0, a1);
+    }
+
+    // ---- 5. sum this CTA's slice of the O columns over the cluster
+    cluster_sync();
+    const int cols = (Dv + C - 1) / C;
+    const int c0 = (int)crank * cols, c1 = min(Dv, c0 + cols);
+    for (int e = t; e < R * max(0, c1 - c0); e += kThreads) {
+        const int r = e / (c1 - c0), d = c0 + e % (c1 - c0);
+        float part[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) part[c] = ld_peer(peer_addr(&op[r * Dv + d], (uint32_t)c));
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) acc += part[c];
+        const bool dead = lse_s[r] == -CUDART_INF_F;
+        T* orow = static_cast<T*>(p.o) + b * p.so0 + row_h[r] * p.so1 + (long long)row_i[r] * p.so2;
+        orow[d] = from_f<T>(dead ? 0.f : acc);
+    }
+    if (crank == 0 && p.lse && t < R) {
+        const float L = lse_s[t];
+        p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
+    }
+    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+}
+
+int elem_bytes(int dt) { return dt == kF32 ? 4 : 2; }
+
+// Cluster size and chunk for a problem, and the shared-memory bytes it needs.
+void plan(const Problem& p, int* C, int* chunk, DecParams* dp, int* smem) {
+    int c = (int)((p.Skv + 127) / 128);
+    c = c < 1 ? 1 : (c > kMaxCluster ? kMaxCluster : c);
+    *C = c;
+    *chunk = (int)((p.Skv + c - 1) / c);
+    const int rows = (int)(p.group * p.Sq);
+    int off = 0;
+    dp->off_v = off; off += *chunk * (int)p.Dv * elem_bytes(p.dtype); off = (off + 15) & ~15;
+    dp->off_q = off; off += rows * (int)p.D * 4; off = (off + 15) & ~15;
+    dp->off_s = off; off += rows * *chunk * 4; off = (off + 15) & ~15;
+    dp->off_o = off; off += rows * (int)p.Dv * 4; off = (off + 15) & ~15;
+    dp->off_stat = off; off += rows * 2 * 4;
+    *smem = off;
+}
+
+bool aligned16(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+std::mutex g_mu;
+struct Ready { const void* kern; int dev; };
+Ready g_ready[32];
+int g_nready = 0;
+
+template <typename T, int RM>
+cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
+    DecParams p;
+    std::memset(&p, 0, sizeof(p));
+    int C, chunk, smem;
+    plan(pr, &C, &chunk, &p, &smem);
+    p.q = pr.q; p.sq0 = pr.sq[0]; p.sq1 = pr.sq[1]; p.sq2 = pr.sq[2];
+    p.k = pr.k; p.sk0 = pr.sk[0]; p.sk1 = pr.sk[1]; p.sk2 = pr.sk[2];
+    p.v = pr.v; p.sv0 = pr.sv[0]; p.sv1 = pr.sv[1]; p.sv2 = pr.sv[2];
+    p.mask = pr.mask; p.mask_kind = pr.mask_kind; p.mask_dtype = pr.mask_dtype;
+    p.sm0 = pr.sm[0]; p.sm1 = pr.sm[1]; p.sm2 = pr.sm[2];
+    p.o = pr.o; p.so0 = pr.so[0]; p.so1 = pr.so[1]; p.so2 = pr.so[2];
+    p.p = pr.p; p.sp0 = pr.sp[0]; p.sp1 = pr.sp[1]; p.sp2 = pr.sp[2];
+    p.lse = pr.lse;
+    p.Hq = (int)pr.Hq; p.Sq = (int)pr.Sq; p.Skv = (int)pr.Skv; p.D = (int)pr.D; p.Dv = (int)pr.Dv;
+    p.group = (int)pr.group; p.rows = (int)(pr.group * pr.Sq); p.chunk = chunk; p.causal = pr.causal;
+    p.c2 = pr.scale * kLog2e;
+
+    auto kern = decode_kernel<T, RM>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        // once per (kernel, device): opt in to the shared-memory budget
+        std::lock_guard<std::mutex> lock(g_mu);
+        bool ready = false;
+        for (int i = 0; i < g_nready; ++i)
+            ready |= g_ready[i].kern == reinterpret_cast<const void*>(kern) && g_ready[i].dev == dev;
+        if (!ready) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+            if (e != cudaSuccess) return e;
+            if (g_nready < 32) g_ready[g_nready++] = Ready{reinterpret_cast<const void*>(kern), dev};
+        }
+    }
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)C, (unsigned)pr.Hkv, (unsigned)pr.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
+    const int64_t rows = p.group * p.Sq;
+    if (rows <= 4) return launch_rm<T, 4>(p, stream);
+    if (rows <= 8) return launch_rm<T, 8>(p, stream);
+    return launch_rm<T, 16>(p, stream);
+}
+
+}  // namespace
+
+bool decode_supports(const Problem& p, const char** why) {
+    if (p.group * p.Sq > kMaxRows) { *why = "more than 16 query rows per key/value head"; return false; }
+    if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
+    if (p.D > 256 || p.Dv > 256) { *why = "head dim above 256"; return false; }
+    if (p.B > 65535 || p.Hkv > 65535 || p.Skv >= (1ll << 31)) { *why = "sizes beyond the grid limits"; return false; }
+    const int es = elem_bytes(p.dtype);
+    if ((p.D * es) % 16 != 0 || (p.Dv * es) % 16 != 0) { *why = "head dims must be 16-byte multiples"; return false; }
+    if (!aligned16(p.k) || !aligned16(p.v) || (p.sk[2] * es) % 16 != 0 || (p.sv[2] * es) % 16 != 0 ||
+        (p.Hkv > 1 && ((p.sk[1] * es) % 16 != 0 || (p.sv[1] * es) % 16 != 0)) ||
+        (p.B > 1 && ((p.sk[0] * es) % 16 != 0 || (p.sv[0] * es) % 16 != 0))) {
+        *why = "k and v rows must be 16-byte aligned"; return false;
+    }
+    int C, chunk, smem;
+    DecParams dp;
+    plan(p, &C, &chunk, &dp, &smem);
+    if (chunk > kThreads) { *why = "more than 2048 keys (one thread per key of a chunk)"; return false; }
+    if (smem > kSmemBudget) { *why = "key chunk too long for shared memory"; return false; }
+    return true;
+}
+
+cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {
+    const char* why;
+    if (!decode_supports(p, &why)) return cudaErrorNotSupported;
+    switch (p.dtype) {
+        case kF32: return launch_t<float>(p, stream);
+        case kF16: return launch_t<__half>(p, stream);
+        case kBF16: return launch_t<__nv_bfloat16>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 }  // namespace sdpa
