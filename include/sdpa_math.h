@@ -82,7 +82,8 @@ typedef enum {
     SDPA_VARIANT_SIMT = 1,       /* CUDA-core kernel: any dtype, D <= 256, any layout */
     SDPA_VARIANT_TC_TWOPASS = 2, /* tcgen05: row-LSE sweep, then exact P = exp(S - lse) and P V */
     SDPA_VARIANT_TC_FUSED = 3,   /* tcgen05: one sweep, the whole score row block kept in TMEM */
-    SDPA_VARIANT_DECODE = 4      /* few query rows per KV head: KV split across a CTA cluster */
+    SDPA_VARIANT_DECODE = 4,     /* few query rows per KV head: KV split across a CTA cluster */
+    SDPA_VARIANT_TC_PAIRED = 5   /* TC_TWOPASS with two query tiles per CTA sharing each K/V load */
 } sdpa_variant;
 
 typedef struct {
@@ -151,9 +152,12 @@ typedef struct {
  * family the call would use.  The variant is chosen by the number of score
  * tiles that survive causal truncation, not by area (the page's fusion
  * criterion, "single-kernel fusion (small shapes)" update), with thresholds
- * set for GB300.  `requested` is the variant the caller would pass to
- * sdpa_math_fwd_ex (AUTO = let the rule choose).  Data pointers are checked
- * for NULL and alignment but never dereferenced.
+ * set for GB300.  Between the two tensor-core two-pass layouts it picks
+ * TC_PAIRED (two query tiles per CTA) when the paired grid still gives about
+ * one CTA per SM, else TC_TWOPASS.  `requested` is the variant the caller
+ * would pass to sdpa_math_fwd_ex (AUTO = let the rule choose).  Data pointers
+ * are checked for NULL and alignment but never dereferenced; the only CUDA
+ * call is a query of the current device's SM count (nothing is enqueued).
  */
 sdpa_status sdpa_math_plan(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
                            const sdpa_tensor *mask, sdpa_mask_kind mask_kind, int is_causal,

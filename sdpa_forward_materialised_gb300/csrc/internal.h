@@ -46,7 +46,11 @@ inline int64_t live_tiles_per_slice(int64_t Sq, int64_t Skv, bool causal) {
 // (then it returns cudaErrorNotSupported without launching).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 bool tc_supports(const Problem& p, bool fused, const char** why);
-cudaError_t launch_tc(const Problem& p, bool fused, cudaStream_t stream);
+// mode 1: two-pass kernel, one 128-row query tile per CTA; 2: two-pass kernel,
+// two query tiles per CTA; 3: fused single-sweep kernel.
+cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream);
+// Query tiles per CTA that suit the two-pass kernel for p (1 or 2).
+int tc_query_tiles(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 

@@ -31,13 +31,14 @@ sdpa_status fail(sdpa_status s, const char* fmt, ...) {
     return s;
 }
 
-// SDPA_MATH_VARIANT=auto|simt|twopass|fused|decode, read once at load.
+// SDPA_MATH_VARIANT=auto|simt|twopass|paired|fused|decode, read once at load.
 sdpa_variant env_variant() {
     static const sdpa_variant v = [] {
         const char* e = std::getenv("SDPA_MATH_VARIANT");
         if (!e || !*e || !std::strcmp(e, "auto")) return SDPA_VARIANT_AUTO;
         if (!std::strcmp(e, "simt")) return SDPA_VARIANT_SIMT;
         if (!std::strcmp(e, "twopass")) return SDPA_VARIANT_TC_TWOPASS;
+        if (!std::strcmp(e, "paired")) return SDPA_VARIANT_TC_PAIRED;
         if (!std::strcmp(e, "fused")) return SDPA_VARIANT_TC_FUSED;
         if (!std::strcmp(e, "decode")) return SDPA_VARIANT_DECODE;
         return SDPA_VARIANT_AUTO;
@@ -201,7 +202,8 @@ sdpa_variant choose(const sdpa::Problem& p) {
     if (p.dtype == SDPA_F32) return SDPA_VARIANT_SIMT;
     if (sdpa::decode_supports(p, &why)) return SDPA_VARIANT_DECODE;
     if (p.Skv <= kFusedMaxKeys && sdpa::tc_supports(p, true, &why)) return SDPA_VARIANT_TC_FUSED;
-    if (sdpa::tc_supports(p, false, &why)) return SDPA_VARIANT_TC_TWOPASS;
+    if (sdpa::tc_supports(p, false, &why))
+        return sdpa::tc_query_tiles(p) == 2 ? SDPA_VARIANT_TC_PAIRED : SDPA_VARIANT_TC_TWOPASS;
     return SDPA_VARIANT_SIMT;
 }
 
@@ -212,6 +214,7 @@ sdpa_status resolve(const sdpa::Problem& p, sdpa_variant requested, sdpa_variant
         case SDPA_VARIANT_AUTO: *out = choose(p); return SDPA_OK;
         case SDPA_VARIANT_SIMT: *out = v; return SDPA_OK;
         case SDPA_VARIANT_TC_TWOPASS:
+        case SDPA_VARIANT_TC_PAIRED:
         case SDPA_VARIANT_TC_FUSED:
             if (!sdpa::tc_supports(p, v == SDPA_VARIANT_TC_FUSED, &why))
                 return fail(SDPA_ERR_UNSUPPORTED, "tensor-core variant cannot serve this call: %s", why);
@@ -270,8 +273,9 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (chosen) {
-        case SDPA_VARIANT_TC_TWOPASS: e = sdpa::launch_tc(p, false, st); break;
-        case SDPA_VARIANT_TC_FUSED: e = sdpa::launch_tc(p, true, st); break;
+        case SDPA_VARIANT_TC_TWOPASS: e = sdpa::launch_tc(p, 1, st); break;
+        case SDPA_VARIANT_TC_PAIRED: e = sdpa::launch_tc(p, 2, st); break;
+        case SDPA_VARIANT_TC_FUSED: e = sdpa::launch_tc(p, 3, st); break;
         case SDPA_VARIANT_DECODE: e = sdpa::launch_decode(p, st); break;
         default: e = sdpa::launch_simt(p, st); break;
     }

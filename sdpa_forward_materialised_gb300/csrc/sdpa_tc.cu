@@ -60,7 +60,7 @@ constexpr int kThreads = 384;
 // gives registers up, the two softmax warpgroups take them.  The launch must
 // provide at least 128*kRegsLow + 256*kRegsHigh registers per CTA (checked on
 // the host before the first launch; setmaxnreg.inc would otherwise wait forever).
-constexpr uint32_t kRegsLow = 72, kRegsHigh = 200;
+constexpr uint32_t kRegsLow = 72, kRegsHigh = 208;
 
 // The three outer tensor-map dimensions are stored in stride order; a packed
 // code (2 bits per slot) says which logical dimension (1 = rows, 2 = head,
@@ -80,7 +80,7 @@ struct TcParams {
     float* lse;
     void* p;  // P (the zero tiles above a causal diagonal are written with plain stores)
     long long sp0, sp1, sp2;
-    uint32_t ord_q, ord_k, ord_v, ord_p;
+    uint32_t ord_q, ord_k, ord_v, ord_p, ord_o;
 };
 
 // Bounded mbarrier wait.  Returns false (after recording the first failure
@@ -200,22 +200,25 @@ __device__ __forceinline__ void store_p_row(const uint32_t (&hp)[64], uint32_t t
     }
 }
 
-// NCOL output columns of this thread's row from TMEM to global (16-byte stores).
-template <typename T, int NCOL>
-__device__ __forceinline__ void store_o_cols(uint32_t taddr, T* dst, bool row_ok, bool dead) {
+// NCHUNK 64-column chunks of this thread's O row, from TMEM (fp32) into the
+// 128B-swizzled staging tile (chunk c of row t at buf + c*16 KB + t*128,
+// 16-byte unit u at u ^ (t % 8)), rounded to dtype; zeros for a dead row.
+template <typename T, int NCHUNK>
+__device__ __forceinline__ void stage_o_row(uint32_t taddr, uint32_t buf, int t, bool dead) {
 #pragma unroll
-    for (int c = 0; c < NCOL / 32; ++c) {
-        float ov[32];
-        tmem_ld32(taddr + c * 32, ov);
-        if (row_ok) {
+    for (int c = 0; c < NCHUNK; ++c) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float ov[32];
+            tmem_ld32(taddr + c * 64 + half * 32, ov);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                uint4 pk;
-                pk.x = Pack<T>::two(dead ? 0.f : ov[u * 8 + 0], dead ? 0.f : ov[u * 8 + 1]);
-                pk.y = Pack<T>::two(dead ? 0.f : ov[u * 8 + 2], dead ? 0.f : ov[u * 8 + 3]);
-                pk.z = Pack<T>::two(dead ? 0.f : ov[u * 8 + 4], dead ? 0.f : ov[u * 8 + 5]);
-                pk.w = Pack<T>::two(dead ? 0.f : ov[u * 8 + 6], dead ? 0.f : ov[u * 8 + 7]);
-                *reinterpret_cast<uint4*>(dst + c * 32 + u * 8) = pk;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = Pack<T>::two(dead ? 0.f : ov[u * 8 + 2 * e], dead ? 0.f : ov[u * 8 + 2 * e + 1]);
+                const int unit = half * 4 + u;
+                st_shared_v4(buf + c * 16384 + t * 128 + ((unit ^ (t % 8)) * 16), w[0], w[1], w[2], w[3]);
             }
         }
     }
@@ -230,6 +233,18 @@ __device__ __forceinline__ void warp_store_p(const CUtensorMap* tm, uint32_t ord
     const int row = r0 + 32 * w;
     for (int c = 0; c < 2; ++c)
         tma_store_4d(tm, tile_base + c * 16384 + w * 32 * 128, kv0 + 64 * c, pick(ord & 3, row, h, b),
+                     pick((ord >> 2) & 3, row, h, b), pick((ord >> 4) & 3, row, h, b));
+    bulk_commit();
+}
+
+// Per-warp O store: NCHUNK boxes of 64 columns x 32 rows from the staging
+// tile, starting at output column col0.
+template <int NCHUNK>
+__device__ __forceinline__ void warp_store_o(const CUtensorMap* tm, uint32_t ord, uint32_t buf, int w, int col0,
+                                             int r0, int h, int b) {
+    const int row = r0 + 32 * w;
+    for (int c = 0; c < NCHUNK; ++c)
+        tma_store_4d(tm, buf + c * 16384 + w * 32 * 128, col0 + 64 * c, pick(ord & 3, row, h, b),
                      pick((ord >> 2) & 3, row, h, b), pick((ord >> 4) & 3, row, h, b));
     bulk_commit();
 }
@@ -252,16 +267,19 @@ __device__ __forceinline__ void zero_p_region(const TcParams& prm, int b, int h,
 
 __device__ __forceinline__ void softmax_group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
-template <int D>
+template <int D, int QT>
 struct TcCfg {
     static constexpr int kChunks = D / 64;               // 128-byte (64-element) column chunks
     static constexpr int kTileBytes = 128 * D * 2;        // one Q / K / V tile
-    static constexpr int kStages = (D == 64) ? 8 : 4;     // K/V ring depth
     static constexpr int kPBytes = 128 * 128 * 2;         // one P tile (2 chunks)
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffKV = kOffQ + kTileBytes;
-    static constexpr int kOffP = kOffKV + kStages * kTileBytes;
-    static constexpr int kOffStats = kOffP + 2 * kPBytes;  // float[2][128]: group 1's (m, l), then the lse
+    static constexpr int kBarBytes = 256;                 // mbarriers, TMEM slot, abort flag
+    static constexpr int kFixed = QT * kTileBytes + 2 * kPBytes + 2 * 128 * 4 + kBarBytes + 1024;
+    static constexpr int kMaxSmem = 227 * 1024;
+    static constexpr int kStages = (kMaxSmem - kFixed) / kTileBytes > 8 ? 8 : (kMaxSmem - kFixed) / kTileBytes;
+    static constexpr int kOffQ = 0;                        // QT query tiles
+    static constexpr int kOffKV = kOffQ + QT * kTileBytes;
+    static constexpr int kOffP = kOffKV + kStages * kTileBytes;  // one P tile per stream
+    static constexpr int kOffStats = kOffP + 2 * kPBytes;        // float[2][128]: stream 1's (m, l), then lse
     static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
     // barrier indices
     static constexpr int bQ = 0;
@@ -273,18 +291,53 @@ struct TcCfg {
     static constexpr int bPV = bPF + 2;          // [2] P buffer consumed by P V (MMA commit)
     static constexpr int bO = bPV + 2;           // O complete (MMA commit)
     static constexpr int kBars = bO + 1;
-    static constexpr int kSmem = kOffBar + kBars * 8 + 16 + 1024;  // + tmem slot, abort flag, alignment slack
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kTmemO = 256;
+    static constexpr uint32_t kTmemO = 256;  // O of stream s at kTmemO + s * D (QT == 2), else kTmemO
+    static_assert(kBars * 8 + 16 <= kBarBytes, "barrier block");
+    static_assert(kStages >= 2, "K/V ring too shallow");
+    static_assert(kSmem <= kMaxSmem, "shared memory budget");
+    static_assert(kTmemO + (QT == 2 ? 2 * D : D) <= kTmemCols, "TMEM budget");
 };
 
-template <int D, typename T, bool kMasked>
+// Which query tile(s) a CTA owns and which key tiles each of its two softmax
+// streams handles.
+//   QT == 1: one 128-row query tile; stream s takes the key tiles j with
+//            j % 2 == s (the two streams alternate over the S / P buffers and
+//            merge their row statistics after sweep 1).
+//   QT == 2: two query tiles of one (batch, head) that share every K / V tile
+//            load; stream s owns query tile s and all of its live key tiles.
+//            With a causal mask the tiles are paired (i, n-1-i), so every
+//            pair holds the same number of live score tiles.
+template <int QT>
+struct Work {
+    int q[2];      // query tile of each stream (-1: stream idle), QT == 2
+    int n[2];      // live key tiles of each stream's query tile
+    int n_kv;      // key tiles the CTA walks
+    // does stream s take key tile j?
+    __device__ __forceinline__ bool handles(int s, int j) const {
+        if constexpr (QT == 2) return j < n[s];
+        else return (j & 1) == s && j < n_kv;
+    }
+    __device__ __forceinline__ int qtile(int s) const { return QT == 2 ? q[s] : q[0]; }
+};
+
+__device__ __forceinline__ int live_tiles(const TcParams& p, int qt) {
+    if (qt < 0) return 0;
+    const int n_all = (p.Skv + 127) / 128;
+    if (!p.causal) return n_all;
+    const int r_last = min(qt * 128 + 127, p.Sq - 1);
+    return min(r_last, p.Skv - 1) / 128 + 1;
+}
+
+template <int D, typename T, bool kMasked, int QT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_p,
-                  const TcParams prm) {
-    using C = TcCfg<D>;
+                  const __grid_constant__ CUtensorMap tm_o, const TcParams prm) {
+    using C = TcCfg<D, QT>;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr int L = QT == 1 ? 2 : 1;  // sweep-2 lookahead of Q K^T over P V, in key tiles
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (128B-swizzle atoms)
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -299,12 +352,22 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = blockIdx.x, b = blockIdx.y;
-    const int qt = prm.n_qtiles - 1 - (int)blockIdx.z;  // heaviest causal tiles first
-    const int r0 = qt * 128;
     const int hk = h / prm.group;
-    const int r_last = min(r0 + 127, prm.Sq - 1);
-    const int n_all = (prm.Skv + 127) / 128;
-    const int n_live = prm.causal ? (min(r_last, prm.Skv - 1) / 128 + 1) : n_all;
+    Work<QT> wk;
+    if constexpr (QT == 2) {
+        wk.q[0] = blockIdx.z;
+        wk.q[1] = prm.n_qtiles - 1 - (int)blockIdx.z;
+        if (wk.q[1] <= wk.q[0]) wk.q[1] = -1;  // the middle tile of an odd count runs alone
+        wk.n[0] = live_tiles(prm, wk.q[0]);
+        wk.n[1] = live_tiles(prm, wk.q[1]);
+        wk.n_kv = max(wk.n[0], wk.n[1]);
+    } else {
+        wk.q[0] = prm.n_qtiles - 1 - (int)blockIdx.z;  // heaviest causal tiles first
+        wk.q[1] = -1;
+        wk.n[0] = wk.n[1] = live_tiles(prm, wk.q[0]);
+        wk.n_kv = wk.n[0];
+    }
+    const int n_kv = wk.n_kv;
 
     // ------------------------------------------------------------ set-up
     if (threadIdx.x == 0) {
@@ -332,10 +395,15 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            mbar_arrive_expect_tx(bar(C::bQ), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sQ + c * 16384, &tm_q, bar(C::bQ), c * 64, pick(prm.ord_q & 3, r0, h, b),
-                            pick((prm.ord_q >> 2) & 3, r0, h, b), pick((prm.ord_q >> 4) & 3, r0, h, b));
+            const int nq = (QT == 2 && wk.q[1] >= 0) ? 2 : 1;
+            mbar_arrive_expect_tx(bar(C::bQ), nq * C::kTileBytes);
+            for (int s = 0; s < nq; ++s) {
+                const int r0 = wk.q[s] * 128;
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sQ + s * C::kTileBytes + c * 16384, &tm_q, bar(C::bQ), c * 64,
+                                pick(prm.ord_q & 3, r0, h, b), pick((prm.ord_q >> 2) & 3, r0, h, b),
+                                pick((prm.ord_q >> 4) & 3, r0, h, b));
+            }
             int it = 0;
             auto load = [&](const CUtensorMap* tm, uint32_t ord, int kv0) {
                 const int s = it % C::kStages;
@@ -348,12 +416,12 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                 pick((ord >> 4) & 3, kv0, hk, b));
                 ++it;
             };
-            // the MMA issuer consumes: K_0..K_{n-1} (sweep 1); then K_0, K_1 and,
-            // for each j, K_{j+2} (when it exists) followed by V_j (sweep 2)
-            for (int j = 0; j < n_live; ++j) load(&tm_k, prm.ord_k, j * 128);
-            for (int j = 0; j < min(2, n_live); ++j) load(&tm_k, prm.ord_k, j * 128);
-            for (int j = 0; j < n_live; ++j) {
-                if (j + 2 < n_live) load(&tm_k, prm.ord_k, (j + 2) * 128);
+            // the MMA issuer consumes: K_0..K_{n-1} (sweep 1); then K_0..K_{L-1}
+            // and, for each j, K_{j+L} (when it exists) followed by V_j (sweep 2)
+            for (int j = 0; j < n_kv; ++j) load(&tm_k, prm.ord_k, j * 128);
+            for (int j = 0; j < min(L, n_kv); ++j) load(&tm_k, prm.ord_k, j * 128);
+            for (int j = 0; j < n_kv; ++j) {
+                if (j + L < n_kv) load(&tm_k, prm.ord_k, (j + L) * 128);
                 load(&tm_v, prm.ord_v, j * 128);
             }
         } else if (warp == 1 && lane == 0) {
@@ -361,132 +429,179 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
             constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
             wait_bar(bar(C::bQ), 0, abort_flag, 2, C::bQ);
-            int it = 0, sc = 0;
-            int pv_use0 = 0, pv_use1 = 0;
-            auto qk = [&]() {
-                const int s = it % C::kStages;
-                wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
-                const int buf = sc & 1;
-                wait_bar(bar(C::bSE + buf), ((sc >> 1) & 1) ^ 1, abort_flag, 2, C::bSE + buf);
-                tc_fence_after();
-                const uint32_t d = tmem + buf * 128;
+            int it = 0;
+            int s_use[2] = {0, 0}, p_use[2] = {0, 0};
+            bool o_init[2] = {false, false};
+            // S_s = Q_s K_j^T for every stream that handles key tile j
+            auto qk = [&](int j) {
+                const int st = it % C::kStages;
+                wait_bar(bar(C::bKVF + st), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + st);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    tc_mma_f16(d, sw128_desc(sQ + off, 16, 1024),
-                               sw128_desc(sKV + s * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                for (int s = 0; s < 2; ++s) {
+                    if (!wk.handles(s, j)) continue;
+                    wait_bar(bar(C::bSE + s), (s_use[s] & 1) ^ 1, abort_flag, 2, C::bSE + s);
+                    tc_fence_after();
+                    const uint32_t qbase = sQ + (QT == 2 ? s : 0) * C::kTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        tc_mma_f16(tmem + s * 128, sw128_desc(qbase + off, 16, 1024),
+                                   sw128_desc(sKV + st * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                    tc_commit(bar(C::bSF + s));
+                    ++s_use[s];
                 }
-                tc_commit(bar(C::bKVE + s));
-                tc_commit(bar(C::bSF + buf));
+                tc_commit(bar(C::bKVE + st));
                 ++it;
-                ++sc;
             };
+            // O_s += P_s V_j for every stream that handles key tile j
             auto pv = [&](int j) {
-                const int pb = (n_live + j) & 1;  // sweep-2 tile j lives in S / P buffer (n + j) mod 2
-                const int use = pb ? pv_use1++ : pv_use0++;
-                wait_bar(bar(C::bPF + pb), use & 1, abort_flag, 2, C::bPF + pb);
-                const int s = it % C::kStages;
-                wait_bar(bar(C::bKVF + s), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + s);
-                tc_fence_after();
+                const int st = it % C::kStages;
+                wait_bar(bar(C::bKVF + st), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + st);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;  // P: K-major, 16 keys per step
-                    const uint32_t b_off = kk * 2048;                         // V: N-major, 16 key rows per step
-                    tc_mma_f16(tmem + C::kTmemO, sw128_desc(sP + pb * C::kPBytes + a_off, 16, 1024),
-                               sw128_desc(sKV + s * C::kTileBytes + b_off, 16384, 1024), idesc_pv,
-                               (j > 0 || kk > 0) ? 1u : 0u);
+                for (int s = 0; s < 2; ++s) {
+                    if (!wk.handles(s, j)) continue;
+                    wait_bar(bar(C::bPF + s), p_use[s] & 1, abort_flag, 2, C::bPF + s);
+                    tc_fence_after();
+                    const int o = QT == 2 ? s : 0;
+                    const uint32_t od = tmem + C::kTmemO + o * D;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;  // P: K-major, 16 keys per step
+                        const uint32_t b_off = kk * 2048;                         // V: N-major, 16 key rows per step
+                        tc_mma_f16(od, sw128_desc(sP + s * C::kPBytes + a_off, 16, 1024),
+                                   sw128_desc(sKV + st * C::kTileBytes + b_off, 16384, 1024), idesc_pv,
+                                   (o_init[o] || kk > 0) ? 1u : 0u);
+                    }
+                    o_init[o] = true;
+                    tc_commit(bar(C::bPV + s));
+                    ++p_use[s];
                 }
-                tc_commit(bar(C::bKVE + s));
-                tc_commit(bar(C::bPV + pb));
+                tc_commit(bar(C::bKVE + st));
                 ++it;
             };
-            // sweep 1, then sweep 2 with S two tiles ahead of P V, so that the
-            // scores a softmax group needs next never wait behind the other
-            // group's P tile
-            for (int j = 0; j < n_live; ++j) qk();
-            for (int j = 0; j < min(2, n_live); ++j) qk();
-            for (int j = 0; j < n_live; ++j) {
-                if (j + 2 < n_live) qk();
+            // sweep 1, then sweep 2 with Q K^T L tiles ahead of P V, so that the
+            // scores a softmax stream needs next are computed while it writes P
+            for (int j = 0; j < n_kv; ++j) qk(j);
+            for (int j = 0; j < min(L, n_kv); ++j) qk(j);
+            for (int j = 0; j < n_kv; ++j) {
+                if (j + L < n_kv) qk(j + L);
                 pv(j);
             }
             tc_commit(bar(C::bO));
         } else if (warp >= 2) {
             // ------------------------------------------------------------ causal zero tiles
-            zero_p_region(prm, b, h, r0, r_last + 1, n_live * 128, warp - 2, 2, lane);
+            for (int s = 0; s < QT; ++s) {
+                const int qt = wk.qtile(s);
+                if (qt < 0) continue;
+                const int r0 = qt * 128;
+                zero_p_region(prm, b, h, r0, min(r0 + 128, prm.Sq), wk.n[s] * 128, warp - 2, 2, lane);
+            }
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         setmaxnreg_inc<kRegsHigh>();
-        const int wg = (warp - 4) >> 2;           // owns S buffer wg and P buffer wg
+        const int sid = (warp - 4) >> 2;          // stream: S buffer, P buffer, barriers
         const int t = (threadIdx.x - 128) & 127;  // row within the tile == TMEM lane
-        const int row = r0 + t;
-        const bool row_ok = row < prm.Sq;
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_tmem = tmem + lane_base + wg * 128;
-        const float cexp = kMasked ? 1.f : prm.c2;
-        float s[128];
+        const int qt = wk.qtile(sid);
+        if (qt >= 0) {
+            const int r0 = qt * 128;
+            const int row = r0 + t;
+            const bool row_ok = row < prm.Sq;
+            const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+            const uint32_t s_tmem = tmem + lane_base + sid * 128;
+            const float cexp = kMasked ? 1.f : prm.c2;
+            float s[128];
+            int s_use = 0;
 
-        auto load_s = [&](int sc, int role) {
-            wait_bar(bar(C::bSF + wg), (sc >> 1) & 1, abort_flag, role, C::bSF + wg);
+            auto load_s = [&](int role) {
+                wait_bar(bar(C::bSF + sid), s_use & 1, abort_flag, role, C::bSF + sid);
+                tc_fence_after();
+                tmem_ld128(s_tmem, s);
+                tc_fence_before();
+                mbar_arrive(bar(C::bSE + sid));
+                ++s_use;
+            };
+
+            // sweep 1: this stream's score tiles -> row max / sum of exp2
+            float m = -CUDART_INF_F, l = 0.f;
+            for (int j = 0; j < n_kv; ++j) {
+                if (!wk.handles(sid, j)) continue;
+                load_s(4);
+                mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+                tile_stats(s, cexp, m, l);
+            }
+            float lse2;
+            if constexpr (QT == 1) {
+                // merge the two streams' statistics: stream 1 publishes (m, l),
+                // stream 0 forms the row lse and publishes it, stream 1 reads it
+                // back (both then hold bit-identical values)
+                if (sid == 1) {
+                    stat[t] = m;
+                    stat[128 + t] = l;
+                }
+                softmax_group_sync();
+                if (sid == 0) {
+                    const float m1 = stat[t], l1 = stat[128 + t];
+                    const float mm = fmaxf(m, m1);
+                    stat[t] = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(l * ex2(m - mm) + l1 * ex2(m1 - mm));
+                }
+                softmax_group_sync();
+                lse2 = stat[t];
+            } else {
+                lse2 = (m == -CUDART_INF_F) ? -CUDART_INF_F : m + log2f(l);
+            }
+            const bool dead = lse2 == -CUDART_INF_F;
+            const float neg_lse = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
+            if (lane == 0) {
+                prefetch_tmap(&tm_p);
+                prefetch_tmap(&tm_o);
+            }
+
+            // sweep 2: exact P into this stream's swizzled shared tile, then TMA stores
+            int p_use = 0;
+            for (int j = 0; j < n_kv; ++j) {
+                if (!wk.handles(sid, j)) continue;
+                load_s(5);
+                mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+                uint32_t hp[64];
+                tile_probs<T>(s, cexp, neg_lse, hp);
+                wait_bar(bar(C::bPV + sid), (p_use & 1) ^ 1, abort_flag, 5, C::bPV + sid);
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+                store_p_row(hp, sP + sid * C::kPBytes, t);
+                fence_proxy_async_smem();
+                mbar_arrive(bar(C::bPF + sid));
+                __syncwarp();
+                if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + sid * C::kPBytes, warp & 3, j * 128, r0, h, b);
+                ++p_use;
+            }
+            if (lane == 0) bulk_wait0();  // the P tile is read out before O reuses it
+            __syncwarp();
+
+            // epilogue: O rows from TMEM into this stream's (now idle) P tile,
+            // then per-warp TMA stores.  QT == 2: all D columns; QT == 1: stream s
+            // takes the 64-column chunk s (D = 128), or stream 0 all 64 (D = 64).
+            wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
             tc_fence_after();
-            tmem_ld128(s_tmem, s);
-            tc_fence_before();
-            mbar_arrive(bar(C::bSE + wg));
-        };
-
-        // sweep 1: this group's score tiles -> partial row max / sum of exp2
-        float m = -CUDART_INF_F, l = 0.f;
-        for (int sc = wg; sc < n_live; sc += 2) {
-            load_s(sc, 4);
-            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, sc * 128);
-            tile_stats(s, cexp, m, l);
+            const uint32_t obuf = sP + sid * C::kPBytes;
+            const uint32_t o_tmem = tmem + lane_base + C::kTmemO + (QT == 2 ? sid * D : 0);
+            if constexpr (QT == 2) {
+                stage_o_row<T, D / 64>(o_tmem, obuf, t, dead);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) warp_store_o<D / 64>(&tm_o, prm.ord_o, obuf, warp & 3, 0, r0, h, b);
+            } else if (D == 128 || sid == 0) {
+                const int c0 = D == 128 ? sid : 0;
+                stage_o_row<T, 1>(o_tmem + 64 * c0, obuf, t, dead);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) warp_store_o<1>(&tm_o, prm.ord_o, obuf, warp & 3, 64 * c0, r0, h, b);
+            }
+            if (lane == 0) bulk_wait0();
+            if ((QT == 2 || sid == 0) && prm.lse && row_ok)
+                prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
         }
-        // merge the two groups' statistics: group 1 publishes (m, l), group 0
-        // forms the row lse and publishes it, group 1 reads it back (both groups
-        // then hold bit-identical values)
-        if (wg == 1) {
-            stat[t] = m;
-            stat[128 + t] = l;
-        }
-        softmax_group_sync();
-        if (wg == 0) {
-            const float m1 = stat[t], l1 = stat[128 + t];
-            const float mm = fmaxf(m, m1);
-            stat[t] = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(l * ex2(m - mm) + l1 * ex2(m1 - mm));
-        }
-        softmax_group_sync();
-        const float lse2 = stat[t];
-        const bool dead = lse2 == -CUDART_INF_F;
-        const float neg_lse = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
-        if (lane == 0) prefetch_tmap(&tm_p);
-
-        // sweep 2: exact P into this group's swizzled shared tile, then TMA stores
-        int use = 0;
-        for (int sc = n_live + ((wg - n_live) & 1); sc < 2 * n_live; sc += 2) {
-            const int j = sc - n_live;
-            load_s(sc, 5);
-            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
-            uint32_t hp[64];
-            tile_probs<T>(s, cexp, neg_lse, hp);
-            wait_bar(bar(C::bPV + wg), (use & 1) ^ 1, abort_flag, 5, C::bPV + wg);
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
-            store_p_row(hp, sP + wg * C::kPBytes, t);
-            fence_proxy_async_smem();
-            mbar_arrive(bar(C::bPF + wg));
-            __syncwarp();
-            if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + wg * C::kPBytes, warp & 3, j * 128, r0, h, b);
-            ++use;
-        }
-        if (lane == 0) bulk_wait0();
-
-        // epilogue: this group's half of the O columns
-        wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
-        tc_fence_after();
-        T* orow = static_cast<T*>(prm.o) + b * prm.so0 + h * prm.so1 + (long long)row * prm.so2;
-        store_o_cols<T, D / 2>(tmem + lane_base + C::kTmemO + wg * (D / 2), orow + wg * (D / 2), row_ok, dead);
-        if (wg == 0 && prm.lse && row_ok)
-            prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
     }
 
     // ------------------------------------------------------------ teardown
@@ -637,16 +752,17 @@ cudaError_t prepare_kernel(K kern, int smem) {
     return state == 1 ? cudaSuccess : cudaErrorNotSupported;
 }
 
-template <int D, typename T, bool kMasked>
+template <int D, typename T, bool kMasked, int QT>
 cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
-    using C = TcCfg<D>;
-    CUtensorMap mq, mk, mv, mp;
+    using C = TcCfg<D, QT>;
+    CUtensorMap mq, mk, mv, mp, mo;
     TcParams prm;
     std::memset(&prm, 0, sizeof(prm));
     if (!make_map(&mq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, 128, &prm.ord_q) ||
         !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, 128, &prm.ord_k) ||
         !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 128, &prm.ord_v) ||
-        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 32, &prm.ord_p))
+        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 32, &prm.ord_p) ||
+        !make_map(&mo, p.dtype, p.o, p.Dv, p.Sq, p.Hq, p.B, p.so, 32, &prm.ord_o))
         return cudaErrorNotSupported;
     prm.Sq = (int)p.Sq;
     prm.Skv = (int)p.Skv;
@@ -664,19 +780,50 @@ cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
     prm.lse = p.lse;
     prm.p = p.p;
     prm.sp0 = p.sp[0]; prm.sp1 = p.sp[1]; prm.sp2 = p.sp[2];
-    auto kern = tc_twopass_kernel<D, T, kMasked>;
+    auto kern = tc_twopass_kernel<D, T, kMasked, QT>;
     cudaError_t e = prepare_kernel(kern, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)prm.n_qtiles);
-    kern<<<grid, kThreads, C::kSmem, stream>>>(mq, mk, mv, mp, prm);
+    const unsigned nz = QT == 2 ? (unsigned)((prm.n_qtiles + 1) / 2) : (unsigned)prm.n_qtiles;
+    dim3 grid((unsigned)p.Hq, (unsigned)p.B, nz);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(mq, mk, mv, mp, mo, prm);
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
+int sm_count() {
+    static int n = [] {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return 148;
+        return v;
+    }();
+    return n;
+}
+
+}  // namespace
+
+// Query tiles per CTA: two tiles share every K / V load (half the load traffic
+// per score tile) when that still gives about one CTA per SM; otherwise one.
+int tc_query_tiles(const Problem& p) {
+    const int64_t nq = (p.Sq + 127) / 128;
+    if (nq < 2) return 1;
+    const int64_t pairs = p.B * p.Hq * ((nq + 1) / 2);
+    return pairs * 4 >= (int64_t)sm_count() * 3 ? 2 : 1;
+}
+
+namespace {
+
+template <typename T, int QT>
+cudaError_t launch_qt(const Problem& p, cudaStream_t stream) {
     const bool masked = p.mask_kind != kMaskNone;
-    if (p.D == 64) return masked ? launch_twopass<64, T, true>(p, stream) : launch_twopass<64, T, false>(p, stream);
-    return masked ? launch_twopass<128, T, true>(p, stream) : launch_twopass<128, T, false>(p, stream);
+    if (p.D == 64)
+        return masked ? launch_twopass<64, T, true, QT>(p, stream) : launch_twopass<64, T, false, QT>(p, stream);
+    return masked ? launch_twopass<128, T, true, QT>(p, stream) : launch_twopass<128, T, false, QT>(p, stream);
+}
+
+template <typename T>
+cudaError_t launch_t(const Problem& p, int qtiles, cudaStream_t stream) {
+    return qtiles == 2 ? launch_qt<T, 2>(p, stream) : launch_qt<T, 1>(p, stream);
 }
 
 }  // namespace
@@ -701,10 +848,10 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
     return true;
 }
 
-cudaError_t launch_tc(const Problem& p, bool fused, cudaStream_t stream) {
+cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream) {
     const char* why;
-    if (!tc_supports(p, fused, &why)) return cudaErrorNotSupported;
-    return p.dtype == kF16 ? launch_t<__half>(p, stream) : launch_t<__nv_bfloat16>(p, stream);
+    if (mode < 1 || mode > 3 || !tc_supports(p, mode == 3, &why)) return cudaErrorNotSupported;
+    return p.dtype == kF16 ? launch_t<__half>(p, mode, stream) : launch_t<__nv_bfloat16>(p, mode, stream);
 }
 
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int* value) {

@@ -68,7 +68,7 @@ def _full_check(q, k, v, mask, causal, scale, variant="auto", check_lse=True):
 def _variants_for(q, k, v, mask, causal):
     """Every kernel family that accepts this call (the SIMT one always does)."""
     out = []
-    for name in ("simt", "twopass", "fused", "decode"):
+    for name in ("simt", "twopass", "paired", "fused", "decode"):
         try:
             sm.sdpa_math_plan(q, k, v, mask, is_causal=causal, variant=name)
             out.append(name)
