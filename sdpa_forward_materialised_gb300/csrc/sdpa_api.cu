@@ -194,7 +194,7 @@ sdpa_status validate(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
 
 // Live-tile threshold below which the single-sweep fused tensor-core kernel is
 // used (score row blocks of at most 512 keys fit the 512 TMEM columns).
-constexpr int64_t kFusedMaxKeys = 512;
+constexpr int64_t kFusedMaxKeys = 256;
 
 // Variant the AUTO rule picks for a validated problem.
 sdpa_variant choose(const sdpa::Problem& p) {

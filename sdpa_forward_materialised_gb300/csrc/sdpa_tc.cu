@@ -143,11 +143,32 @@ template <typename T, bool kMasked>
 __device__ __forceinline__ void mask_tile(float (&s)[128], const TcParams& prm, int b, int h, int row,
                                           bool row_ok, int kv0) {
     if constexpr (kMasked) {
+        const int n = row_ok ? min(128, prm.Skv - kv0) : 0;  // keys of this row inside the tile
+        const unsigned char* mrow = static_cast<const unsigned char*>(prm.mask) + b * prm.sm0 + h * prm.sm1 +
+                                    (long long)row * prm.sm2 + kv0;
+        if (prm.mask_kind == kMaskBool && n > 0 && (reinterpret_cast<uintptr_t>(mrow) & 3) == 0) {
+            // bool mask: four keys per 32-bit load (the per-key byte loads of a
+            // row-per-thread layout would each cost a separate memory request)
 #pragma unroll
-        for (int x = 0; x < 128; ++x) {
-            const int key = kv0 + x;
-            const float add = (row_ok && key < prm.Skv) ? mask_term<T>(prm, b, h, row, key) : -CUDART_INF_F;
-            s[x] = fmaf(s[x], prm.c2, add);
+            for (int w = 0; w < 32; ++w) {
+                uint32_t m4 = 0;
+                if (4 * w + 4 <= n) {
+                    m4 = *reinterpret_cast<const uint32_t*>(mrow + 4 * w);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * w + e < n) m4 |= static_cast<uint32_t>(mrow[4 * w + e]) << (8 * e);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s[4 * w + e] = ((m4 >> (8 * e)) & 0xffu) ? fmaf(s[4 * w + e], prm.c2, 0.f) : -CUDART_INF_F;
+            }
+        } else {
+#pragma unroll
+            for (int x = 0; x < 128; ++x) {
+                const float add = x < n ? mask_term<T>(prm, b, h, row, kv0 + x) : -CUDART_INF_F;
+                s[x] = fmaf(s[x], prm.c2, add);
+            }
         }
     }
     int lim = prm.Skv - 1 - kv0;  // last visible key offset in this tile
@@ -617,6 +638,323 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- fused single-sweep kernel
+// Small key counts (Skv <= 256: at most two 128-key score tiles per row
+// block): S for every key of the row block stays in TMEM, so the row max, the
+// sum of exponentials and P = exp(S - lse) all come from one Q K^T, and the
+// whole forward is one launch with no second sweep (the small-shape fused
+// variant of the page's "single-kernel fusion (small shapes)" update).
+//
+// One CTA (256 threads, two warpgroups) per 128-row query tile of one
+// (batch, head).  Q, K and V arrive by asynchronous 16-byte copies straight in
+// the 128B-swizzled operand layout (any row stride that keeps rows 16-byte
+// aligned); a bool mask tile is staged in shared memory with coalesced loads;
+// warpgroup w owns key tile w.  P goes to the swizzled A-operand tile of P V,
+// from which warps copy it to global memory row by row with coalesced stores
+// that follow the alignment of the caller's P rows (a 100-key row of 200 bytes
+// is fine).  Every wait is bounded.
+struct FusedIO {
+    const void* q; long long sq0, sq1, sq2;
+    const void* k; long long sk0, sk1, sk2;
+    const void* v; long long sv0, sv1, sv2;
+    uint32_t tmem_cols;  // power of two >= S columns + D
+};
+
+struct FusedCfg {
+    static constexpr int kThreads = 256;
+    static constexpr int kMaxKeyTiles = 2;
+};
+
+template <int D>
+struct FusedSmem {
+    static constexpr int kTile = 128 * D * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kTile;
+    static constexpr int kOffV = kOffK + FusedCfg::kMaxKeyTiles * kTile;
+    static constexpr int kOffP = kOffV + FusedCfg::kMaxKeyTiles * kTile;
+    static constexpr int kEnd = kOffP + FusedCfg::kMaxKeyTiles * 128 * 128 * 2;
+    // float[2 (max, sum)][2 warpgroups][128]; aliases K, which is dead once S is in TMEM
+    static constexpr int kOffStat = kOffK;
+    // bool mask tile [128 rows][kMaskPitch bytes] (odd word pitch: conflict-free
+    // row-per-thread reads); after the statistics in the dead K tiles when they
+    // have room, else in its own region
+    static constexpr int kMaskPitch = 260;
+    static constexpr int kMaskBytes = 128 * kMaskPitch;
+    static constexpr bool kMaskInK = 2048 + kMaskBytes <= FusedCfg::kMaxKeyTiles * kTile;
+    static constexpr int kOffMask = kMaskInK ? kOffK + 2048 : kEnd;
+    static constexpr int kOffBar = kMaskInK ? kEnd : kEnd + kMaskBytes;
+    static constexpr int kSmem = kOffBar + 64 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// Rows [0, nvalid) of a [rows, X] slice (element row stride srow, rows
+// 16-byte aligned) into a 128-row 128B-swizzled tile with asynchronous 16-byte
+// copies (all in flight together); rows past nvalid are zero-filled.
+template <typename T>
+__device__ __forceinline__ void load_tile_sw128(uint32_t dst, const T* src, long long srow, int nvalid, int X) {
+    const int upr = X / 8;  // 16-byte units per row
+    for (int u = threadIdx.x; u < 128 * upr; u += FusedCfg::kThreads) {
+        const int r = u / upr, c = u % upr;
+        const bool ok = r < nvalid;
+        const T* g = ok ? src + r * srow + c * 8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         dst + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                     "l"(g), "r"(ok ? 16 : 0)
+                     : "memory");
+    }
+}
+
+template <int D, typename T, bool kMasked>
+__global__ void __launch_bounds__(FusedCfg::kThreads, 1)
+tc_fused_kernel(const TcParams prm, const FusedIO io) {
+    using L = FusedSmem<D>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sQ = smem_u32(smem + L::kOffQ), sK = smem_u32(smem + L::kOffK);
+    const uint32_t sV = smem_u32(smem + L::kOffV), sP = smem_u32(smem + L::kOffP);
+    float* stat = reinterpret_cast<float*>(smem + L::kOffStat);  // [2 (max, sum)][2 warpgroups][128]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [0] S ready, [1] O ready
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32;
+    const int h = blockIdx.x, b = blockIdx.y, qt = blockIdx.z;
+    const int hk = h / prm.group;
+    const int r0 = qt * 128;
+    const int n_kv = (prm.Skv + 127) / 128;  // 1 or 2
+    const uint32_t kTmemO = n_kv * 128;      // O columns follow the S tiles
+
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bars[0]), 1);
+        mbar_init(smem_u32(&bars[1]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), io.tmem_cols);
+        tmem_relinquish();
+    }
+    // Q tile, K and V tiles -> swizzled operand tiles
+    const T* Q = static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2;
+    load_tile_sw128<T>(sQ, Q, io.sq2, min(128, prm.Sq - r0), D);
+    for (int j = 0; j < n_kv; ++j) {
+        const T* K = static_cast<const T*>(io.k) + b * io.sk0 + hk * io.sk1 + (long long)(j * 128) * io.sk2;
+        const T* V = static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1 + (long long)(j * 128) * io.sv2;
+        const int nv = min(128, prm.Skv - j * 128);
+        load_tile_sw128<T>(sK + j * L::kTile, K, io.sk2, nv, D);
+        load_tile_sw128<T>(sV + j * L::kTile, V, io.sv2, nv, D);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // S_j = Q K_j^T for both key tiles, one commit
+    if (threadIdx.x == 0) {
+        constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
+        for (int j = 0; j < n_kv; ++j)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                tc_mma_f16(tmem + j * 128, sw128_desc(sQ + off, 16, 1024),
+                           sw128_desc(sK + j * L::kTile + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+        tc_commit(smem_u32(&bars[0]));
+    }
+
+    const int wg = threadIdx.x / 128, t = threadIdx.x % 128;
+    const int row = r0 + t;
+    const bool row_ok = row < prm.Sq;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const bool mine = wg < n_kv;  // this warpgroup owns key tile wg
+    const float cexp = kMasked ? 1.f : prm.c2;
+    float s[128];
+    // A bool mask is read once per CTA with coalesced loads (warp w takes rows
+    // w, w+8, ...; lanes take consecutive 4-byte words, or bytes when the rows
+    // are not 4-byte aligned) and staged in shared memory; the loads are issued
+    // before S is ready, the stores after (the staging area may alias K).
+    constexpr int kMaskRowsPerWarp = 16;
+    uint32_t mreg[kMaskRowsPerWarp][2];
+    const bool stage_mask = kMasked && prm.mask_kind == kMaskBool;
+    const unsigned char* mbase = static_cast<const unsigned char*>(prm.mask) + b * prm.sm0 + h * prm.sm1;
+    const bool m_words = stage_mask && ((reinterpret_cast<uintptr_t>(mbase) | (uintptr_t)prm.sm2) & 3) == 0;
+    if (stage_mask) {
+        const int lane = threadIdx.x % 32;
+#pragma unroll
+        for (int i = 0; i < kMaskRowsPerWarp; ++i) {
+            const int rr = warp + 8 * i, grow = r0 + rr;
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+                uint32_t v = 0;
+                if (grow < prm.Sq) {
+                    const unsigned char* mr = mbase + (long long)grow * prm.sm2;
+                    if (m_words) {
+                        const int k4 = 4 * (lane + 32 * hw);
+                        if (k4 + 4 <= prm.Skv) v = *reinterpret_cast<const uint32_t*>(mr + k4);
+                        else
+                            for (int e = 0; e < 4; ++e)
+                                if (k4 + e < prm.Skv) v |= static_cast<uint32_t>(mr[k4 + e]) << (8 * e);
+                    } else {
+                        const int k1 = lane + 32 * hw;  // bytes: keys k1, k1 + 64, k1 + 128, k1 + 192
+                        for (int e = 0; e < 4; ++e)
+                            if (k1 + 64 * e < prm.Skv) v |= static_cast<uint32_t>(mr[k1 + 64 * e]) << (8 * e);
+                    }
+                }
+                mreg[i][hw] = v;
+            }
+        }
+    }
+    wait_bar(smem_u32(&bars[0]), 0, abort_flag, 7, 0);
+    tc_fence_after();
+    const uint32_t sMask = smem_u32(smem + L::kOffMask);
+    if (stage_mask) {
+        const int lane = threadIdx.x % 32;
+#pragma unroll
+        for (int i = 0; i < kMaskRowsPerWarp; ++i) {
+            const int rr = warp + 8 * i;
+#pragma unroll
+            for (int hw = 0; hw < 2; ++hw) {
+                const uint32_t v = mreg[i][hw];
+                if (m_words) {
+                    asm volatile("st.shared.b32 [%0], %1;" ::"r"(sMask + rr * L::kMaskPitch + 4 * (lane + 32 * hw)), "r"(v)
+                                 : "memory");
+                } else {
+                    const int k1 = lane + 32 * hw;
+                    for (int e = 0; e < 4; ++e)
+                        asm volatile("st.shared.u8 [%0], %1;" ::"r"(sMask + rr * L::kMaskPitch + k1 + 64 * e),
+                                     "r"((v >> (8 * e)) & 0xffu)
+                                     : "memory");
+                }
+            }
+        }
+        __syncthreads();
+    }
+    float mt = -CUDART_INF_F;
+    if (mine) {
+        tmem_ld128(tmem + lane_base + wg * 128, s);
+        if (stage_mask) {
+            // keys of this row from the staged tile (zero bytes past Skv / Sq)
+            const uint32_t mrow = sMask + t * L::kMaskPitch + wg * 128;
+#pragma unroll
+            for (int w = 0; w < 32; ++w) {
+                uint32_t m4;
+                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(m4) : "r"(mrow + 4 * w));
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s[4 * w + e] = ((m4 >> (8 * e)) & 0xffu) ? fmaf(s[4 * w + e], prm.c2, 0.f) : -CUDART_INF_F;
+            }
+            mask_tile<T, false>(s, prm, b, h, row, row_ok, wg * 128);  // ragged keys / rows
+        } else {
+            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, wg * 128);
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
+        mt = mx * cexp;
+    }
+    stat[wg * 128 + t] = mt;
+    __syncthreads();
+    const float m = fmaxf(stat[t], stat[128 + t]);
+    float lpart = 0.f;
+    if (mine && m != -CUDART_INF_F) {
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int x = 0; x < 128; ++x) acc[x & 7] += ex2(fmaf(s[x], cexp, -m));
+        lpart = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    }
+    stat[256 + wg * 128 + t] = lpart;
+    __syncthreads();
+    const float l = stat[256 + t] + stat[384 + t];
+    const float lse2 = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
+    const bool dead = lse2 == -CUDART_INF_F;
+    uint32_t hp[64];
+    if (mine) {
+        tile_probs<T>(s, cexp, dead ? -CUDART_INF_F : -lse2, hp);
+        store_p_row(hp, sP + wg * 128 * 128 * 2, t);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        tc_fence_after();
+        constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
+        for (int j = 0; j < n_kv; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;
+                const uint32_t b_off = kk * 2048;
+                tc_mma_f16(tmem + kTmemO, sw128_desc(sP + j * 128 * 128 * 2 + a_off, 16, 1024),
+                           sw128_desc(sV + j * L::kTile + b_off, 16384, 1024), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+        tc_commit(smem_u32(&bars[1]));
+    }
+    // P rows to global memory while P V runs: warp w copies rows w, w+8, ...
+    // out of the swizzled tiles; lanes take consecutive key pairs (4-byte
+    // stores) or, when the caller's P rows are only 2-byte aligned, keys
+    {
+        const int lane = threadIdx.x % 32;
+        const int nrows = min(128, prm.Sq - r0);
+        for (int rr = warp; rr < nrows; rr += 8) {
+            uint16_t* prow = static_cast<uint16_t*>(prm.p) + b * prm.sp0 + h * prm.sp1 + (long long)(r0 + rr) * prm.sp2;
+            auto src = [&](int key) {  // shared address of P[rr, key]
+                const int kt = key & 127;
+                return sP + (key >> 7) * (128 * 128 * 2) + (kt >> 6) * 16384 + rr * 128 +
+                       ((((kt >> 3) & 7) ^ (rr & 7)) << 4) + (kt & 7) * 2;
+            };
+            if ((reinterpret_cast<uintptr_t>(prow) & 3) == 0) {
+                for (int key = 2 * lane; key < prm.Skv; key += 64) {
+                    uint32_t v;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src(key)));
+                    if (key + 1 < prm.Skv) *reinterpret_cast<uint32_t*>(prow + key) = v;
+                    else prow[key] = static_cast<uint16_t>(v);
+                }
+            } else {
+                for (int key = lane; key < prm.Skv; key += 32) {
+                    uint16_t v;
+                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(src(key)));
+                    prow[key] = v;
+                }
+            }
+        }
+    }
+    wait_bar(smem_u32(&bars[1]), 0, abort_flag, 7, 1);
+    tc_fence_after();
+    // O: warpgroup w writes columns [w D/2, (w+1) D/2) of its rows
+    {
+        T* orow = static_cast<T*>(prm.o) + b * prm.so0 + h * prm.so1 + (long long)row * prm.so2 + wg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            float ov[32];
+            tmem_ld32(tmem + lane_base + kTmemO + wg * (D / 2) + c * 32, ov);
+            if (row_ok) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 pk;
+                    pk.x = Pack<T>::two(dead ? 0.f : ov[u * 8 + 0], dead ? 0.f : ov[u * 8 + 1]);
+                    pk.y = Pack<T>::two(dead ? 0.f : ov[u * 8 + 2], dead ? 0.f : ov[u * 8 + 3]);
+                    pk.z = Pack<T>::two(dead ? 0.f : ov[u * 8 + 4], dead ? 0.f : ov[u * 8 + 5]);
+                    pk.w = Pack<T>::two(dead ? 0.f : ov[u * 8 + 6], dead ? 0.f : ov[u * 8 + 7]);
+                    *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = pk;
+                }
+            }
+        }
+    }
+    if (wg == 0 && prm.lse && row_ok)
+        prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        if (*abort_flag)
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        tmem_dealloc(tmem, io.tmem_cols);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -729,7 +1067,7 @@ Prepared g_prep[64];
 int g_prep_n = 0;
 
 template <typename K>
-cudaError_t prepare_kernel(K kern, int smem) {
+cudaError_t prepare_kernel(K kern, int smem, bool reg_split = true) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -743,7 +1081,7 @@ cudaError_t prepare_kernel(K kern, int smem) {
     if (e != cudaSuccess) return e;
     int state = 1;
     // the in-kernel register split must fit what the launch allocates
-    if (fa.numRegs * kThreads < (int)(128 * kRegsLow + 256 * kRegsHigh)) state = 2;
+    if (reg_split && fa.numRegs * kThreads < (int)(128 * kRegsLow + 256 * kRegsHigh)) state = 2;
     if (state == 1) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
@@ -789,6 +1127,42 @@ cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+template <int D, typename T, bool kMasked>
+cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
+    using L = FusedSmem<D>;
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    prm.Sq = (int)p.Sq;
+    prm.Skv = (int)p.Skv;
+    prm.Hq = (int)p.Hq;
+    prm.group = (int)p.group;
+    prm.n_qtiles = (int)((p.Sq + 127) / 128);
+    prm.causal = p.causal;
+    prm.c2 = p.scale * kLog2e;
+    prm.mask = p.mask;
+    prm.mask_kind = p.mask_kind;
+    prm.mask_dtype = p.mask_dtype;
+    prm.sm0 = p.sm[0]; prm.sm1 = p.sm[1]; prm.sm2 = p.sm[2];
+    prm.o = p.o;
+    prm.so0 = p.so[0]; prm.so1 = p.so[1]; prm.so2 = p.so[2];
+    prm.lse = p.lse;
+    prm.p = p.p;
+    prm.sp0 = p.sp[0]; prm.sp1 = p.sp[1]; prm.sp2 = p.sp[2];
+    FusedIO io;
+    std::memset(&io, 0, sizeof(io));
+    io.q = p.q; io.sq0 = p.sq[0]; io.sq1 = p.sq[1]; io.sq2 = p.sq[2];
+    io.k = p.k; io.sk0 = p.sk[0]; io.sk1 = p.sk[1]; io.sk2 = p.sk[2];
+    io.v = p.v; io.sv0 = p.sv[0]; io.sv1 = p.sv[1]; io.sv2 = p.sv[2];
+    const uint32_t need = (uint32_t)((p.Skv + 127) / 128 * 128 + D);
+    io.tmem_cols = need <= 256 ? 256u : 512u;
+    auto kern = tc_fused_kernel<D, T, kMasked>;
+    cudaError_t e = prepare_kernel(kern, L::kSmem, false);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)prm.n_qtiles);
+    kern<<<grid, FusedCfg::kThreads, L::kSmem, stream>>>(prm, io);
+    return cudaGetLastError();
+}
+
 int sm_count() {
     static int n = [] {
         int dev = 0, v = 0;
@@ -822,14 +1196,18 @@ cudaError_t launch_qt(const Problem& p, cudaStream_t stream) {
 }
 
 template <typename T>
-cudaError_t launch_t(const Problem& p, int qtiles, cudaStream_t stream) {
-    return qtiles == 2 ? launch_qt<T, 2>(p, stream) : launch_qt<T, 1>(p, stream);
+cudaError_t launch_t(const Problem& p, int mode, cudaStream_t stream) {
+    if (mode == 3) {
+        const bool masked = p.mask_kind != kMaskNone;
+        if (p.D == 64) return masked ? launch_fused<64, T, true>(p, stream) : launch_fused<64, T, false>(p, stream);
+        return masked ? launch_fused<128, T, true>(p, stream) : launch_fused<128, T, false>(p, stream);
+    }
+    return mode == 2 ? launch_qt<T, 2>(p, stream) : launch_qt<T, 1>(p, stream);
 }
 
 }  // namespace
 
 bool tc_supports(const Problem& p, bool fused, const char** why) {
-    if (fused) { *why = "the fused single-sweep kernel is not built yet"; return false; }
     if (p.dtype != kF16 && p.dtype != kBF16) { *why = "dtype must be f16 or bf16"; return false; }
     if (p.D != p.Dv || (p.D != 64 && p.D != 128)) { *why = "head dim must be 64 or 128 (D == Dv)"; return false; }
     if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
@@ -837,10 +1215,22 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
     if (p.Sq >= (1ll << 31) || p.Skv >= (1ll << 31) || p.B > 65535 || p.Sq > 65535ll * 128) {
         *why = "sizes beyond the grid limits"; return false;
     }
+    const int64_t eq[3] = {p.B, p.Hq, p.Sq}, ek[3] = {p.B, p.Hkv, p.Skv};
+    if (fused) {
+        // plain 16-byte loads of q / k / v rows and stores of O rows; P rows
+        // may have any alignment
+        if (p.Skv > 256) { *why = "the fused kernel keeps at most 256 keys in TMEM"; return false; }
+        if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o)) {
+            *why = "q, k, v and out must be 16-byte aligned"; return false;
+        }
+        if (!strides_ok(p.sq, eq) || !strides_ok(p.sk, ek) || !strides_ok(p.sv, ek) || !strides_ok(p.so, eq)) {
+            *why = "q, k, v and out rows must start on 16-byte boundaries"; return false;
+        }
+        return true;
+    }
     if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.p) || !aligned16(p.o)) {
         *why = "q, k, v, out and probs must be 16-byte aligned"; return false;
     }
-    const int64_t eq[3] = {p.B, p.Hq, p.Sq}, ek[3] = {p.B, p.Hkv, p.Skv};
     if (!strides_ok(p.sq, eq) || !strides_ok(p.sk, ek) || !strides_ok(p.sv, ek) || !strides_ok(p.sp, eq) ||
         !strides_ok(p.so, eq)) {
         *why = "outer strides must be multiples of 8 elements (16 bytes)"; return false;

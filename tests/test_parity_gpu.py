@@ -131,6 +131,12 @@ SMALL = [
     (1, 2, 2, 136, 136, 64, "f16", False, "bool"),
     (1, 3, 3, 520, 648, 128, "f16", False, None),
     (2, 2, 2, 129, 1032, 64, "bf16", True, None),
+    # shapes the fused single-sweep kernel takes (Skv <= 256), incl. P rows of
+    # 200 bytes (no TMA) and a single key
+    (2, 4, 2, 130, 256, 128, "f16", True, None),
+    (1, 2, 2, 100, 100, 64, "bf16", False, "bool"),
+    (1, 2, 1, 7, 1, 64, "f16", False, None),
+    (1, 3, 3, 250, 129, 128, "bf16", False, "additive"),
 ]
 
 
