@@ -174,6 +174,17 @@ sdpa_status sdpa_math_plan(const sdpa_tensor *q, const sdpa_tensor *k, const sdp
  */
 sdpa_status sdpa_math_device_status(sdpa_stream_t stream);
 
+/*
+ * sdpa_math_selftest_wait -- diagnostic for the failure path above.  Enqueues
+ * on `stream` one single-thread kernel that waits, through the same bounded
+ * mbarrier wait the tensor-core kernels use, on a barrier nothing ever
+ * arrives at.  The wait runs out after about one second, records role 15 in
+ * the device error word and the kernel returns; no fault, no hang.  A
+ * following sdpa_math_device_status(stream) then returns SDPA_ERR_TIMEOUT.
+ * Returns SDPA_OK, or SDPA_ERR_CUDA if the launch fails.
+ */
+sdpa_status sdpa_math_selftest_wait(sdpa_stream_t stream);
+
 /* Message for the last non-OK status returned on this thread ("" if none). */
 const char *sdpa_math_last_error(void);
 

@@ -23,7 +23,7 @@ from . import _build
 
 __all__ = [
     "sdpa_math", "sdpa_math_fwd", "sdpa_math_fwd_ex", "sdpa_math_plan",
-    "sdpa_math_device_status", "sdpa_math_last_error", "sdpa_math_abi_version",
+    "sdpa_math_device_status", "sdpa_math_selftest_wait", "sdpa_math_last_error", "sdpa_math_abi_version",
     "SdpaError", "SdpaValueError", "load_library", "library_path", "VARIANTS", "STATUS",
 ]
 
@@ -93,6 +93,8 @@ def load_library(build_if_missing: bool = False):
                                        T, T, ctypes.c_int, P(SdpaPlan)]
         lib.sdpa_math_device_status.restype = ctypes.c_int
         lib.sdpa_math_device_status.argtypes = [ctypes.c_void_p]
+        lib.sdpa_math_selftest_wait.restype = ctypes.c_int
+        lib.sdpa_math_selftest_wait.argtypes = [ctypes.c_void_p]
         lib.sdpa_math_last_error.restype = ctypes.c_char_p
         lib.sdpa_math_last_error.argtypes = []
         lib.sdpa_math_abi_version.restype = ctypes.c_int
@@ -211,6 +213,14 @@ def sdpa_math_plan(q, k, v, mask=None, is_causal=False, scale=None, out=None, pr
 def sdpa_math_device_status(stream=None) -> None:
     lib = load_library()
     st = lib.sdpa_math_device_status(_stream_handle(stream))
+    if st != SDPA_OK:
+        _raise(lib, st)
+
+
+def sdpa_math_selftest_wait(stream=None) -> None:
+    """Enqueue the bounded-wait self test (a wait that runs out after ~1 s)."""
+    lib = load_library()
+    st = lib.sdpa_math_selftest_wait(_stream_handle(stream))
     if st != SDPA_OK:
         _raise(lib, st)
 

@@ -57,5 +57,7 @@ cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 // Device error word shared by every kernel of the library (see
 // sdpa_math_device_status).  read_and_clear returns the word's old value.
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int* value);
+// Enqueue the bounded-wait self test (see sdpa_math_selftest_wait).
+cudaError_t launch_selftest_wait(cudaStream_t stream);
 
 }  // namespace sdpa

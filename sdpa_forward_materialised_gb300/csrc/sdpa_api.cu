@@ -315,4 +315,11 @@ sdpa_status sdpa_math_device_status(sdpa_stream_t stream) {
     return SDPA_OK;
 }
 
+sdpa_status sdpa_math_selftest_wait(sdpa_stream_t stream) {
+    g_last_error.clear();
+    const cudaError_t e = sdpa::launch_selftest_wait(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "self-test launch failed: %s", cudaGetErrorString(e));
+    return SDPA_OK;
+}
+
 }  // extern "C"

@@ -1244,6 +1244,28 @@ cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream) {
     return p.dtype == kF16 ? launch_t<__half>(p, mode, stream) : launch_t<__nv_bfloat16>(p, mode, stream);
 }
 
+namespace {
+// One thread waits on an mbarrier that nothing arrives at, through wait_bar:
+// after kWaitLimitCycles the wait records role 15 in the device status word
+// and returns false, and the kernel ends.
+__global__ void selftest_wait_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)wait_bar(smem_u32(&bar), 0, &abort_flag, 15, 0);
+}
+}  // namespace
+
+cudaError_t launch_selftest_wait(cudaStream_t stream) {
+    selftest_wait_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
 cudaError_t status_read_and_clear(cudaStream_t stream, unsigned int* value) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(value, g_status_word, sizeof(unsigned int), 0,
                                               cudaMemcpyDeviceToHost, stream);
