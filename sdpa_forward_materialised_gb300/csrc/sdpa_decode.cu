@@ -127,9 +127,31 @@ decode_kernel(const DecParams p) {
     float* op = reinterpret_cast<float*>(smem + p.off_o);     // [R][Dv] partial O
     float* st = reinterpret_cast<float*>(smem + p.off_stat);  // [R][2] chunk (max, sum)
 
-    // ---- 1. asynchronous copy of the V chunk; query rows as fp32
+    // ---- 1. loads in the order they are needed: the query rows and the first
+    // 128 bytes of this thread's K row into registers, then the V chunk
+    // (asynchronous copies, needed last)
     const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
     const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
+    float qv[RM];  // elements t, t + 256, ... of the [R][D] query block (R * D <= RM * 256)
+#pragma unroll
+    for (int i = 0; i < RM; ++i) {
+        const int e = t + kThreads * i;
+        qv[i] = 0.f;
+        if (e < R * D) {
+            const int r = e / D, d = e % D;
+            const T* qr = static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
+                          (long long)(r % p.Sq) * p.sq2;
+            qv[i] = to_f(qr[d]);
+        }
+    }
+    const uint8_t* krow = reinterpret_cast<const uint8_t*>(K + (long long)t * p.sk2);
+    const int kbytes = D * (int)sizeof(T);
+    uint4 kx[8];
+    if (t < n) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (16 * u < kbytes) kx[u] = __ldg(reinterpret_cast<const uint4*>(krow + 16 * u));
+    }
     {
         const int uv = Dv * (int)sizeof(T) / 16;  // 16-byte units per V row
         for (int u = t; u < n * uv; u += kThreads) {
@@ -142,28 +164,25 @@ decode_kernel(const DecParams p) {
         row_h[t] = hk * p.group + t / p.Sq;
         row_i[t] = t % p.Sq;
     }
-    __syncthreads();
-    for (int e = t; e < R * D; e += kThreads) {
-        const int r = e / D, d = e % D;
-        const T* qr = static_cast<const T*>(p.q) + b * p.sq0 + row_h[r] * p.sq1 + (long long)row_i[r] * p.sq2;
-        qs[r * D + d] = to_f(qr[d]);
-    }
+#pragma unroll
+    for (int i = 0; i < RM; ++i)
+        if (t + kThreads * i < R * D) qs[t + kThreads * i] = qv[i];
     __syncthreads();
 
     // ---- 2. scores: thread j owns key k0 + j and reads its K row straight
-    // into registers, 128 bytes (eight 16-byte loads in flight) per batch
+    // into registers, 128 bytes (eight 16-byte loads in flight) per batch;
+    // the first batch was issued above
     if (t < n) {
-        const uint8_t* krow = reinterpret_cast<const uint8_t*>(K + (long long)t * p.sk2);
-        const int kbytes = D * (int)sizeof(T);
         constexpr int kE = 16 / (int)sizeof(T);  // elements per 16-byte unit
         float acc[RM];
 #pragma unroll
         for (int r = 0; r < RM; ++r) acc[r] = 0.f;
         for (int b0 = 0; b0 < kbytes; b0 += 128) {
-            uint4 kx[8];
+            if (b0 > 0) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (b0 + 16 * u < kbytes) kx[u] = __ldg(reinterpret_cast<const uint4*>(krow + b0 + 16 * u));
+                for (int u = 0; u < 8; ++u)
+                    if (b0 + 16 * u < kbytes) kx[u] = __ldg(reinterpret_cast<const uint4*>(krow + b0 + 16 * u));
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 if (b0 + 16 * u >= kbytes) break;
