@@ -294,14 +294,13 @@ struct TcCfg {
     static constexpr int kTileBytes = 128 * D * 2;        // one Q / K / V tile
     static constexpr int kPBytes = 128 * 128 * 2;         // one P tile (2 chunks)
     static constexpr int kBarBytes = 256;                 // mbarriers, TMEM slot, abort flag
-    static constexpr int kFixed = QT * kTileBytes + 2 * kPBytes + 2 * 128 * 4 + kBarBytes + 1024;
+    static constexpr int kFixed = QT * kTileBytes + 2 * kPBytes + kBarBytes + 1024;
     static constexpr int kMaxSmem = 227 * 1024;
     static constexpr int kStages = (kMaxSmem - kFixed) / kTileBytes > 8 ? 8 : (kMaxSmem - kFixed) / kTileBytes;
     static constexpr int kOffQ = 0;                        // QT query tiles
     static constexpr int kOffKV = kOffQ + QT * kTileBytes;
-    static constexpr int kOffP = kOffKV + kStages * kTileBytes;  // one P tile per stream
-    static constexpr int kOffStats = kOffP + 2 * kPBytes;        // float[2][128]: stream 1's (m, l), then lse
-    static constexpr int kOffBar = kOffStats + 2 * 128 * 4;
+    static constexpr int kOffP = kOffKV + kStages * kTileBytes;  // one P tile per worker
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
     // barrier indices
     static constexpr int bQ = 0;
     static constexpr int bKVF = 1;
@@ -321,26 +320,27 @@ struct TcCfg {
     static_assert(kTmemO + (QT == 2 ? 2 * D : D) <= kTmemCols, "TMEM budget");
 };
 
-// Which query tile(s) a CTA owns and which key tiles each of its two softmax
-// streams handles.
-//   QT == 1: one 128-row query tile; stream s takes the key tiles j with
-//            j % 2 == s (the two streams alternate over the S / P buffers and
-//            merge their row statistics after sweep 1).
-//   QT == 2: two query tiles of one (batch, head) that share every K / V tile
-//            load; stream s owns query tile s and all of its live key tiles.
-//            With a causal mask the tiles are paired (i, n-1-i), so every
-//            pair holds the same number of live score tiles.
+// Which query tile(s) a CTA owns and how its score tiles are shared out.
+// A unit is one 128x128 score tile (query tile s, key tile j); a CTA walks its
+// units in key-tile order (both query tiles of key tile j before key tile
+// j+1, so one K / V load feeds both) and hands each to one of its two softmax
+// warpgroups ("workers"), which owns an S buffer and a P tile.
+//   QT == 1: one 128-row query tile; unit j goes to worker j % 2, and the two
+//            workers merge their row statistics after sweep 1.
+//   QT == 2: two query tiles of one (batch, head); worker s owns query tile s
+//            and all of its units.  (With a causal mask the tiles are paired
+//            (i, n-1-i), which balances CTAs but not workers, so AUTO takes
+//            this layout only without one.)
 template <int QT>
 struct Work {
-    int q[2];      // query tile of each stream (-1: stream idle), QT == 2
-    int n[2];      // live key tiles of each stream's query tile
+    int q[2];      // query tile(s) (q[1] = -1: the CTA has one)
+    int n[2];      // live key tiles of each query tile
     int n_kv;      // key tiles the CTA walks
-    // does stream s take key tile j?
-    __device__ __forceinline__ bool handles(int s, int j) const {
+    // is (query tile s, key tile j) a live unit?
+    __device__ __forceinline__ bool has(int s, int j) const {
         if constexpr (QT == 2) return j < n[s];
-        else return (j & 1) == s && j < n_kv;
+        else return s == 0 && j < n_kv;
     }
-    __device__ __forceinline__ int qtile(int s) const { return QT == 2 ? q[s] : q[0]; }
 };
 
 __device__ __forceinline__ int live_tiles(const TcParams& p, int qt) {
@@ -365,7 +365,6 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const uint32_t sQ = smem_u32(smem + C::kOffQ);
     const uint32_t sKV = smem_u32(smem + C::kOffKV);
     const uint32_t sP = smem_u32(smem + C::kOffP);
-    float* stat = reinterpret_cast<float*>(smem + C::kOffStats);  // [2][128]
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -385,7 +384,8 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         wk.q[0] = prm.n_qtiles - 1 - (int)blockIdx.z;  // heaviest causal tiles first
         wk.q[1] = -1;
-        wk.n[0] = wk.n[1] = live_tiles(prm, wk.q[0]);
+        wk.n[0] = live_tiles(prm, wk.q[0]);
+        wk.n[1] = 0;
         wk.n_kv = wk.n[0];
     }
     const int n_kv = wk.n_kv;
@@ -451,59 +451,67 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
             wait_bar(bar(C::bQ), 0, abort_flag, 2, C::bQ);
             int it = 0;
-            int s_use[2] = {0, 0}, p_use[2] = {0, 0};
-            bool o_init[2] = {false, false};
-            // S_s = Q_s K_j^T for every stream that handles key tile j
+            int s_use0 = 0, s_use1 = 0, p_use0 = 0, p_use1 = 0;  // per worker (scalars: no local memory)
+            bool o_init[2] = {false, false};                     // per query tile
+            int uq = 0, up = 0;                          // units issued (Q K^T / P V) in this sweep
+            // S = Q_s K_j^T for every live unit of key tile j, into its worker's S buffer
             auto qk = [&](int j) {
                 const int st = it % C::kStages;
                 wait_bar(bar(C::bKVF + st), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + st);
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    if (!wk.handles(s, j)) continue;
-                    wait_bar(bar(C::bSE + s), (s_use[s] & 1) ^ 1, abort_flag, 2, C::bSE + s);
+                for (int s = 0; s < QT; ++s) {
+                    if (!wk.has(s, j)) continue;
+                    const int w = QT == 2 ? s : (uq & 1);  // QT == 2: stream s owns query tile s
+                    ++uq;
+                    const int use = w ? s_use1 : s_use0;
+                    wait_bar(bar(C::bSE + w), (use & 1) ^ 1, abort_flag, 2, C::bSE + w);
                     tc_fence_after();
-                    const uint32_t qbase = sQ + (QT == 2 ? s : 0) * C::kTileBytes;
+                    const uint32_t qbase = sQ + s * C::kTileBytes;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        tc_mma_f16(tmem + s * 128, sw128_desc(qbase + off, 16, 1024),
+                        tc_mma_f16(tmem + w * 128, sw128_desc(qbase + off, 16, 1024),
                                    sw128_desc(sKV + st * C::kTileBytes + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
                     }
-                    tc_commit(bar(C::bSF + s));
-                    ++s_use[s];
+                    tc_commit(bar(C::bSF + w));
+                    if (w) ++s_use1;
+                    else ++s_use0;
                 }
                 tc_commit(bar(C::bKVE + st));
                 ++it;
             };
-            // O_s += P_s V_j for every stream that handles key tile j
+            // O_s += P V_j for every live unit of key tile j, from its worker's P tile
             auto pv = [&](int j) {
                 const int st = it % C::kStages;
                 wait_bar(bar(C::bKVF + st), (it / C::kStages) & 1, abort_flag, 2, C::bKVF + st);
 #pragma unroll
-                for (int s = 0; s < 2; ++s) {
-                    if (!wk.handles(s, j)) continue;
-                    wait_bar(bar(C::bPF + s), p_use[s] & 1, abort_flag, 2, C::bPF + s);
+                for (int s = 0; s < QT; ++s) {
+                    if (!wk.has(s, j)) continue;
+                    const int w = QT == 2 ? s : (up & 1);
+                    ++up;
+                    wait_bar(bar(C::bPF + w), (w ? p_use1 : p_use0) & 1, abort_flag, 2, C::bPF + w);
                     tc_fence_after();
-                    const int o = QT == 2 ? s : 0;
-                    const uint32_t od = tmem + C::kTmemO + o * D;
+                    const uint32_t od = tmem + C::kTmemO + s * D;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;  // P: K-major, 16 keys per step
                         const uint32_t b_off = kk * 2048;                         // V: N-major, 16 key rows per step
-                        tc_mma_f16(od, sw128_desc(sP + s * C::kPBytes + a_off, 16, 1024),
+                        tc_mma_f16(od, sw128_desc(sP + w * C::kPBytes + a_off, 16, 1024),
                                    sw128_desc(sKV + st * C::kTileBytes + b_off, 16384, 1024), idesc_pv,
-                                   (o_init[o] || kk > 0) ? 1u : 0u);
+                                   (o_init[s] || kk > 0) ? 1u : 0u);
                     }
-                    o_init[o] = true;
-                    tc_commit(bar(C::bPV + s));
-                    ++p_use[s];
+                    o_init[s] = true;
+                    tc_commit(bar(C::bPV + w));
+                    if (w) ++p_use1;
+                    else ++p_use0;
                 }
                 tc_commit(bar(C::bKVE + st));
                 ++it;
             };
-            // sweep 1, then sweep 2 with Q K^T L tiles ahead of P V, so that the
-            // scores a softmax stream needs next are computed while it writes P
+            // sweep 1, then sweep 2 with Q K^T L key tiles ahead of P V, so that the
+            // scores a worker needs next are computed while it writes P
             for (int j = 0; j < n_kv; ++j) qk(j);
+            uq = 0;
             for (int j = 0; j < min(L, n_kv); ++j) qk(j);
             for (int j = 0; j < n_kv; ++j) {
                 if (j + L < n_kv) qk(j + L);
@@ -513,115 +521,213 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         } else if (warp >= 2) {
             // ------------------------------------------------------------ causal zero tiles
             for (int s = 0; s < QT; ++s) {
-                const int qt = wk.qtile(s);
-                if (qt < 0) continue;
-                const int r0 = qt * 128;
+                if (wk.q[s] < 0) continue;
+                const int r0 = wk.q[s] * 128;
                 zero_p_region(prm, b, h, r0, min(r0 + 128, prm.Sq), wk.n[s] * 128, warp - 2, 2, lane);
             }
         }
     } else {
         // ------------------------------------------------------------ softmax warpgroups
         setmaxnreg_inc<kRegsHigh>();
-        const int sid = (warp - 4) >> 2;          // stream: S buffer, P buffer, barriers
-        const int t = (threadIdx.x - 128) & 127;  // row within the tile == TMEM lane
-        const int qt = wk.qtile(sid);
-        if (qt >= 0) {
-            const int r0 = qt * 128;
-            const int row = r0 + t;
-            const bool row_ok = row < prm.Sq;
+        if constexpr (QT == 2) {
+            // two query tiles: stream s owns query tile s and all of its key tiles
+            // (AUTO takes this layout only without a causal mask, where the two
+            // streams hold the same number of tiles)
+            const int sid = (warp - 4) >> 2;          // stream: S buffer, P buffer, barriers
+            const int t = (threadIdx.x - 128) & 127;  // row within the tile == TMEM lane
+            const int qt = wk.q[sid];
+            if (qt >= 0) {
+                const int r0 = qt * 128;
+                const int row = r0 + t;
+                const bool row_ok = row < prm.Sq;
+                const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+                const uint32_t s_tmem = tmem + lane_base + sid * 128;
+                const float cexp = kMasked ? 1.f : prm.c2;
+                float s[128];
+                int s_use = 0;
+
+                auto load_s = [&](int role) {
+                    wait_bar(bar(C::bSF + sid), s_use & 1, abort_flag, role, C::bSF + sid);
+                    tc_fence_after();
+                    tmem_ld128(s_tmem, s);
+                    tc_fence_before();
+                    mbar_arrive(bar(C::bSE + sid));
+                    ++s_use;
+                };
+
+                // sweep 1: this stream's score tiles -> row max / sum of exp2
+                float m = -CUDART_INF_F, l = 0.f;
+                for (int j = 0; j < n_kv; ++j) {
+                    if (!wk.has(sid, j)) continue;
+                    load_s(4);
+                    mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+                    tile_stats(s, cexp, m, l);
+                }
+                const float lse2 = (m == -CUDART_INF_F) ? -CUDART_INF_F : m + log2f(l);
+                const bool dead = lse2 == -CUDART_INF_F;
+                const float neg_lse = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
+                if (lane == 0) {
+                    prefetch_tmap(&tm_p);
+                    prefetch_tmap(&tm_o);
+                }
+
+                // sweep 2: exact P into this stream's swizzled shared tile, then TMA stores
+                int p_use = 0;
+                for (int j = 0; j < n_kv; ++j) {
+                    if (!wk.has(sid, j)) continue;
+                    load_s(5);
+                    mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+                    uint32_t hp[64];
+                    tile_probs<T>(s, cexp, neg_lse, hp);
+                    wait_bar(bar(C::bPV + sid), (p_use & 1) ^ 1, abort_flag, 5, C::bPV + sid);
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                    store_p_row(hp, sP + sid * C::kPBytes, t);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::bPF + sid));
+                    __syncwarp();
+                    if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + sid * C::kPBytes, warp & 3, j * 128, r0, h, b);
+                    ++p_use;
+                }
+                if (lane == 0) bulk_wait0();  // the P tile is read out before O reuses it
+                __syncwarp();
+
+                // epilogue: O rows (all D columns) from TMEM into this stream's (now
+                // idle) P tile, then per-warp TMA stores
+                wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
+                tc_fence_after();
+                const uint32_t obuf = sP + sid * C::kPBytes;
+                const uint32_t o_tmem = tmem + lane_base + C::kTmemO + sid * D;
+                stage_o_row<T, D / 64>(o_tmem, obuf, t, dead);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) warp_store_o<D / 64>(&tm_o, prm.ord_o, obuf, warp & 3, 0, r0, h, b);
+                if (lane == 0) bulk_wait0();
+                if (prm.lse && row_ok)
+                    prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
+            }
+        } else {
+            const int w = (warp - 4) >> 2;            // worker: S buffer, P tile, barriers
+            const int t = (threadIdx.x - 128) & 127;  // row within a query tile == TMEM lane
             const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-            const uint32_t s_tmem = tmem + lane_base + sid * 128;
+            const uint32_t s_tmem = tmem + lane_base + w * 128;
             const float cexp = kMasked ? 1.f : prm.c2;
             float s[128];
             int s_use = 0;
 
             auto load_s = [&](int role) {
-                wait_bar(bar(C::bSF + sid), s_use & 1, abort_flag, role, C::bSF + sid);
+                wait_bar(bar(C::bSF + w), s_use & 1, abort_flag, role, C::bSF + w);
                 tc_fence_after();
                 tmem_ld128(s_tmem, s);
                 tc_fence_before();
-                mbar_arrive(bar(C::bSE + sid));
+                mbar_arrive(bar(C::bSE + w));
                 ++s_use;
             };
 
-            // sweep 1: this stream's score tiles -> row max / sum of exp2
-            float m = -CUDART_INF_F, l = 0.f;
+            // sweep 1: this worker's units -> partial row max / sum of exp2 per query
+            // tile.  The running pair of each (worker, query tile) lives in the
+            // still idle P tiles, not in registers, so the unit loop carries no
+            // per-tile state (and keeps one copy of its body).
+            float* xs = reinterpret_cast<float*>(smem + C::kOffP);  // [worker][query tile][m, l][128]
+    #pragma unroll
+            for (int q = 0; q < QT; ++q) {
+                xs[((w * QT + q) * 2 + 0) * 128 + t] = -CUDART_INF_F;
+                xs[((w * QT + q) * 2 + 1) * 128 + t] = 0.f;
+            }
+            int u = 0;
             for (int j = 0; j < n_kv; ++j) {
-                if (!wk.handles(sid, j)) continue;
-                load_s(4);
-                mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
-                tile_stats(s, cexp, m, l);
-            }
-            float lse2;
-            if constexpr (QT == 1) {
-                // merge the two streams' statistics: stream 1 publishes (m, l),
-                // stream 0 forms the row lse and publishes it, stream 1 reads it
-                // back (both then hold bit-identical values)
-                if (sid == 1) {
-                    stat[t] = m;
-                    stat[128 + t] = l;
+    #pragma unroll 1
+                for (int q = 0; q < QT; ++q) {
+                    if (!wk.has(q, j)) continue;
+                    if ((u++ & 1) != w) continue;
+                    const int row = (q ? wk.q[1] : wk.q[0]) * 128 + t;
+                    load_s(4);
+                    mask_tile<T, kMasked>(s, prm, b, h, row, row < prm.Sq, j * 128);
+                    float* st = xs + ((w * QT + q) * 2) * 128 + t;
+                    float mq = st[0], lq = st[128];
+                    tile_stats(s, cexp, mq, lq);
+                    st[0] = mq;
+                    st[128] = lq;
                 }
-                softmax_group_sync();
-                if (sid == 0) {
-                    const float m1 = stat[t], l1 = stat[128 + t];
-                    const float mm = fmaxf(m, m1);
-                    stat[t] = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(l * ex2(m - mm) + l1 * ex2(m1 - mm));
-                }
-                softmax_group_sync();
-                lse2 = stat[t];
-            } else {
-                lse2 = (m == -CUDART_INF_F) ? -CUDART_INF_F : m + log2f(l);
             }
-            const bool dead = lse2 == -CUDART_INF_F;
-            const float neg_lse = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
+            // merge the two workers' statistics: both combine the same values in the
+            // same order, so they hold bit-identical lse per row
+            softmax_group_sync();
+            float lse2_0 = -CUDART_INF_F, lse2_1 = -CUDART_INF_F;
+    #pragma unroll
+            for (int q = 0; q < QT; ++q) {
+                const float a0 = xs[((0 * QT + q) * 2 + 0) * 128 + t], b0 = xs[((0 * QT + q) * 2 + 1) * 128 + t];
+                const float a1 = xs[((1 * QT + q) * 2 + 0) * 128 + t], b1 = xs[((1 * QT + q) * 2 + 1) * 128 + t];
+                const float mm = fmaxf(a0, a1);
+                const float v = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(b0 * ex2(a0 - mm) + b1 * ex2(a1 - mm));
+                if (q) lse2_1 = v;
+                else lse2_0 = v;
+            }
+            softmax_group_sync();  // both read the exchange before any P tile is written
             if (lane == 0) {
                 prefetch_tmap(&tm_p);
                 prefetch_tmap(&tm_o);
             }
 
-            // sweep 2: exact P into this stream's swizzled shared tile, then TMA stores
+            // sweep 2: exact P of this worker's units into its swizzled P tile, then TMA stores
             int p_use = 0;
+            u = 0;
+            const float neg0 = lse2_0 == -CUDART_INF_F ? -CUDART_INF_F : -lse2_0;  // a dead row adds -inf: p = 0
+            const float neg1 = lse2_1 == -CUDART_INF_F ? -CUDART_INF_F : -lse2_1;
             for (int j = 0; j < n_kv; ++j) {
-                if (!wk.handles(sid, j)) continue;
-                load_s(5);
-                mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
-                uint32_t hp[64];
-                tile_probs<T>(s, cexp, neg_lse, hp);
-                wait_bar(bar(C::bPV + sid), (p_use & 1) ^ 1, abort_flag, 5, C::bPV + sid);
-                if (lane == 0) bulk_wait_read0();
-                __syncwarp();
-                store_p_row(hp, sP + sid * C::kPBytes, t);
-                fence_proxy_async_smem();
-                mbar_arrive(bar(C::bPF + sid));
-                __syncwarp();
-                if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + sid * C::kPBytes, warp & 3, j * 128, r0, h, b);
-                ++p_use;
+    #pragma unroll 1
+                for (int q = 0; q < QT; ++q) {
+                    if (!wk.has(q, j)) continue;
+                    if ((u++ & 1) != w) continue;
+                    const int r0 = (q ? wk.q[1] : wk.q[0]) * 128, row = r0 + t;
+                    load_s(5);
+                    mask_tile<T, kMasked>(s, prm, b, h, row, row < prm.Sq, j * 128);
+                    uint32_t hp[64];
+                    tile_probs<T>(s, cexp, q ? neg1 : neg0, hp);
+                    wait_bar(bar(C::bPV + w), (p_use & 1) ^ 1, abort_flag, 5, C::bPV + w);
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                    store_p_row(hp, sP + w * C::kPBytes, t);
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(C::bPF + w));
+                    __syncwarp();
+                    if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + w * C::kPBytes, warp & 3, j * 128, r0, h, b);
+                    ++p_use;
+                }
             }
             if (lane == 0) bulk_wait0();  // the P tile is read out before O reuses it
             __syncwarp();
 
-            // epilogue: O rows from TMEM into this stream's (now idle) P tile,
-            // then per-warp TMA stores.  QT == 2: all D columns; QT == 1: stream s
-            // takes the 64-column chunk s (D = 128), or stream 0 all 64 (D = 64).
+            // epilogue: O rows from TMEM into this worker's (now idle) P tile, then
+            // per-warp TMA stores.  QT == 2: worker w writes query tile w (all D
+            // columns); QT == 1: worker w takes the 64-column chunk w (D = 128), or
+            // worker 0 all 64 columns (D = 64).
             wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
             tc_fence_after();
-            const uint32_t obuf = sP + sid * C::kPBytes;
-            const uint32_t o_tmem = tmem + lane_base + C::kTmemO + (QT == 2 ? sid * D : 0);
-            if constexpr (QT == 2) {
-                stage_o_row<T, D / 64>(o_tmem, obuf, t, dead);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) warp_store_o<D / 64>(&tm_o, prm.ord_o, obuf, warp & 3, 0, r0, h, b);
-            } else if (D == 128 || sid == 0) {
-                const int c0 = D == 128 ? sid : 0;
-                stage_o_row<T, 1>(o_tmem + 64 * c0, obuf, t, dead);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) warp_store_o<1>(&tm_o, prm.ord_o, obuf, warp & 3, 64 * c0, r0, h, b);
+            const uint32_t obuf = sP + w * C::kPBytes;
+            const int oq = QT == 2 ? w : 0;  // query tile whose O this worker writes
+            if (wk.q[oq] >= 0) {
+                const int r0 = wk.q[oq] * 128, row = r0 + t;
+                const bool row_ok = row < prm.Sq;
+                const float lse_o = oq ? lse2_1 : lse2_0;
+                const bool dead = lse_o == -CUDART_INF_F;
+                const uint32_t o_tmem = tmem + lane_base + C::kTmemO + oq * D;
+                if constexpr (QT == 2) {
+                    stage_o_row<T, D / 64>(o_tmem, obuf, t, dead);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) warp_store_o<D / 64>(&tm_o, prm.ord_o, obuf, warp & 3, 0, r0, h, b);
+                } else if (D == 128 || w == 0) {
+                    const int c0 = D == 128 ? w : 0;
+                    stage_o_row<T, 1>(o_tmem + 64 * c0, obuf, t, dead);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) warp_store_o<1>(&tm_o, prm.ord_o, obuf, warp & 3, 64 * c0, r0, h, b);
+                }
+                if (lane == 0) bulk_wait0();
+                if ((QT == 2 || w == 0) && prm.lse && row_ok)
+                    prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse_o : lse_o * kLn2;
             }
-            if (lane == 0) bulk_wait0();
-            if ((QT == 2 || sid == 0) && prm.lse && row_ok)
-                prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
         }
     }
 
@@ -1177,10 +1283,12 @@ int sm_count() {
 }  // namespace
 
 // Query tiles per CTA: two tiles share every K / V load (half the load traffic
-// per score tile) when that still gives about one CTA per SM; otherwise one.
+// per score tile) when that still gives about one CTA per SM and there is no
+// causal mask (with one, a paired CTA's two workers hold unequal tile counts
+// and the one-tile layout, whose workers alternate, measured faster).
 int tc_query_tiles(const Problem& p) {
     const int64_t nq = (p.Sq + 127) / 128;
-    if (nq < 2) return 1;
+    if (nq < 2 || p.causal) return 1;
     const int64_t pairs = p.B * p.Hq * ((nq + 1) / 2);
     return pairs * 4 >= (int64_t)sm_count() * 3 ? 2 : 1;
 }
