@@ -153,8 +153,8 @@ typedef struct {
  * tiles that survive causal truncation, not by area (the page's fusion
  * criterion, "single-kernel fusion (small shapes)" update), with thresholds
  * set for GB300.  Between the two tensor-core two-pass layouts it picks
- * TC_PAIRED (two query tiles per CTA) when the paired grid still gives about
- * one CTA per SM, else TC_TWOPASS.  `requested` is the variant the caller
+ * TC_PAIRED (two query tiles per CTA) for calls without a causal mask when the
+ * paired grid still gives about one CTA per SM, else TC_TWOPASS.  `requested` is the variant the caller
  * would pass to sdpa_math_fwd_ex (AUTO = let the rule choose).  Data pointers
  * are checked for NULL and alignment but never dereferenced; the only CUDA
  * call is a query of the current device's SM count (nothing is enqueued).

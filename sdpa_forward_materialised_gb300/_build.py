@@ -51,13 +51,38 @@ def _fingerprint() -> str:
     return h.hexdigest()
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and whitespace (string literals kept)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c == '"':  # string literal: copy up to the closing quote
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            if not c.isspace():
+                out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_fingerprint() -> str:
-    """Hash of the kernel and ABI sources (changes whenever a kernel changes)."""
+    """Hash of the kernel and ABI code (comments and whitespace ignored): it
+    changes whenever a kernel changes, not when its commentary does."""
     h = hashlib.sha256()
     for path in _sources() + _headers():
         h.update(os.path.basename(path).encode())
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

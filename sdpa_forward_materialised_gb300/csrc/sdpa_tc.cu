@@ -1,11 +1,14 @@
-// sdpa_tc.cu -- tcgen05 tensor-core kernel of the materialised-probability
-// SDPA forward (fp16 / bf16, head dim 64 or 128, positive scale).
+// sdpa_tc.cu -- tcgen05 tensor-core kernels of the materialised-probability
+// SDPA forward (fp16 / bf16, head dim 64 or 128, positive scale): the
+// two-pass kernel (one or two 128-row query tiles per CTA) and the fused
+// single-sweep kernel for at most 256 keys.
 //
-// What it computes: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- the
+// What they compute: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- the
 // math backend's (out, attn_probs): P = softmax(scale*QK^T + mask), O = P V,
 // with a fully masked row giving P = O = 0.  P is normalised exactly through
 // the row log-sum-exp, the identity of the page's "P800 exact-P fast path"
-// update (P = exp(scale*QK^T - LSE)), which the kernel evaluates in place:
+// update (P = exp(scale*QK^T - LSE)), which the two-pass kernel evaluates in
+// place:
 //
 //   sweep 1  S_j = Q K_j^T on the tensor cores (TMEM accumulator); running
 //            row max / sum of exp2 in the softmax warps -> lse per row;
@@ -15,18 +18,19 @@
 //            stores of P.  Key tiles above a causal diagonal are never
 //            computed; their P region is written with zeros.
 //
-// One CTA owns a 128-row query tile of one (batch, head); 12 warps:
+// Two-pass kernel: one CTA owns one or two query tiles of one (batch, head);
+// 12 warps:
 //   warp 0       TMA producer (Q once; K tiles; then K/V tiles interleaved)
 //   warp 1       TMEM allocator + single-thread tcgen05.mma issuer
 //   warps 2, 3   zero-fill of the P tiles above the causal diagonal
-//   warps 4..7   softmax warpgroup 0 (score tiles in S buffer 0 / P buffer 0)
-//   warps 8..11  softmax warpgroup 1 (score tiles in S buffer 1 / P buffer 1)
-// Score tiles alternate between the two buffers (tile counter mod 2 over both
-// sweeps).  Each softmax thread owns one query row (its TMEM lane); the groups
-// merge their sweep-1 row statistics through shared memory.  Each softmax
-// warp stores its own 32 rows of every P tile with TMA as soon as it has
-// written them.  After set-up the producer / MMA warpgroup hands registers to
-// the softmax warpgroups.  TMEM: two 128-column S buffers + O (D columns).
+//   warps 4..11  two softmax warpgroups ("workers"), each with its own S
+//                buffer in TMEM and P tile in shared memory
+// Each softmax thread owns one query row (its TMEM lane).  With one query
+// tile the workers alternate over its key tiles and merge their row
+// statistics through shared memory after sweep 1; with two, worker s owns
+// query tile s (see Work).  Each softmax warp stores its own 32 rows of every
+// P tile with TMA as soon as it has written them.  After set-up the producer /
+// MMA warpgroup hands registers to the softmax warpgroups.
 //
 // Every mbarrier wait is bounded: a wait that runs out records itself in the
 // device status word and the CTA unwinds (freeing TMEM) instead of hanging.
