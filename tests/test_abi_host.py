@@ -195,3 +195,30 @@ def test_live_tile_count(lib, Sq, Skv, causal, expect):
 def test_f32_always_plans_simt(lib):
     q, k, v = _qkv(dtype=torch.float32)
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "simt"
+
+
+# AUTO's kernel family per benchmark workload (host-only planning): the fused
+# single-sweep kernel for Skv <= 256, the cluster decode kernel for few rows
+# per KV head, the one-tile two-pass kernel under a causal mask, the paired
+# layout for the non-causal GQA prefill, and the CUDA-core kernel for fp32.
+@pytest.mark.parametrize("name,expect", [
+    ("tiny_f32", "simt"), ("prefill1k_d64_f16", "twopass"), ("prefill2k_d128_f16", "twopass"),
+    ("prefill2k_d128_bf16", "twopass"), ("gqa1k_d128_f16", "paired"), ("decode_skv1152_f16", "decode"),
+    ("tail100_mask_f16", "fused")])
+def test_auto_choice_per_workload(lib, name, expect):
+    from sdpa_forward_materialised_gb300 import workloads as W
+    w = W.BY_NAME[name]
+    q = torch.empty(w.B, w.Hq, w.Sq, w.D, dtype=w.torch_dtype)
+    k = torch.empty(w.B, w.Hkv, w.Skv, w.D, dtype=w.torch_dtype)
+    v = torch.empty(w.B, w.Hkv, w.Skv, w.D, dtype=w.torch_dtype)
+    m = None
+    if w.mask is not None:
+        m = torch.empty(w.B, 1, w.Sq, w.Skv, dtype=torch.bool)
+    assert sm.sdpa_math_plan(q, k, v, m, is_causal=w.is_causal)["variant"] == expect
+
+
+def test_fused_needs_at_most_256_keys(lib):
+    q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=256, D=64)
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "fused"
+    q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=264, D=64)
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant="fused"), "256 keys")
