@@ -62,6 +62,10 @@ def _load():
                 i64, i64, i64, i64, i64, i64, i64,
                 ctypes.c_int, ctypes.c_double, ctypes.POINTER(i64), i64,
                 dp, dp, dp, ctypes.c_int]
+            lib.sdpa_oracle_bwd.restype = ctypes.c_int
+            lib.sdpa_oracle_bwd.argtypes = [
+                dp, dp, dp, dp, dp, dp, i64, i64, i64, i64, i64, i64, i64,
+                ctypes.c_double, dp, dp, dp, ctypes.c_int]
             lib.sdpa_oracle_max_threads.restype = ctypes.c_int
             lib.sdpa_oracle_max_threads.argtypes = []
             _lib = lib
@@ -153,3 +157,34 @@ def oracle_fwd(q, k, v, attn_mask=None, is_causal: bool = False, scale=None,
         return (out.reshape(B, Hq, Sq, Dv), probs.reshape(B, Hq, Sq, Skv),
                 lse.reshape(B, Hq, Sq))
     return out, probs, lse
+
+
+def oracle_bwd(q, k, v, probs, dout, dprobs=None, scale=None, nthreads: int = 1):
+    """(dq, dk, dv) in float64 for L = sum(O * dout) + sum(P * dprobs), given the
+    forward's probability map ``probs`` [B,Hq,Sq,Skv] (see sdpa_oracle_bwd):
+    dS = P * (dP - rowsum(P * dP)) with dP = dout V^T + dprobs; dq = scale dS K,
+    dk = scale dS^T Q and dv = P^T dout, summed over each KV head's query heads."""
+    lib = _load()
+    qd, kd, vd = _as_f64(q), _as_f64(k), _as_f64(v)
+    pd, god = _as_f64(probs), _as_f64(dout)
+    B, Hq, Sq, D = qd.shape
+    Hkv, Skv, Dv = kd.shape[1], kd.shape[2], vd.shape[3]
+    if pd.shape != (B, Hq, Sq, Skv) or god.shape != (B, Hq, Sq, Dv):
+        raise OracleError("probs / dout shapes disagree with q, k, v")
+    gpd = None
+    if dprobs is not None:
+        gpd = _as_f64(dprobs)
+        if gpd.shape != (B, Hq, Sq, Skv):
+            raise OracleError("dprobs must be [B,Hq,Sq,Skv]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D) if D > 0 else 1.0
+    dq = np.zeros((B, Hq, Sq, D), dtype=np.float64)
+    dk = np.zeros((B, Hkv, Skv, D), dtype=np.float64)
+    dv = np.zeros((B, Hkv, Skv, Dv), dtype=np.float64)
+    dummy = np.zeros(1, dtype=np.float64)
+    f = lambda a: _ptr(a if a.size else dummy)
+    rc = lib.sdpa_oracle_bwd(f(qd), f(kd), f(vd), f(pd), f(god), _ptr(gpd) if gpd is not None else None,
+                             B, Hq, Hkv, Sq, Skv, D, Dv, float(scale), f(dq), f(dk), f(dv), int(nthreads))
+    if rc != 0:
+        raise OracleError("oracle rejected the arguments (GQA indivisible or bad sizes)")
+    return dq, dk, dv

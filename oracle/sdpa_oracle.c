@@ -29,7 +29,8 @@
  *
  * Pins: every function here is checked by CPU tests against closed forms,
  * invariants, brute force on tiny inputs and an independent float64 library
- * evaluation (softmax + matmul).
+ * evaluation (softmax + matmul; for the backward, central finite differences
+ * of the forward and float64 autograd).
  */
 #include <math.h>
 #include <stddef.h>
@@ -180,6 +181,95 @@ int sdpa_oracle_fwd(const double *q, const double *k, const double *v,
                            probs + r * Skv, lse + r, s);
         }
         free(s);
+    }
+    return failed ? ORACLE_ERR_ARGUMENT : ORACLE_OK;
+}
+
+/*
+ * sdpa_oracle_bwd -- gradients of the (O, P) forward, given its probability map.
+ *
+ * What it computes (FlagOS-OP PR #10: the overview's A1 item, where gradients
+ * flow through both outputs, dout and dprobs; the "2026-10-07 update: P800
+ * fused backward", where dprobs goes through the exact softmax Jacobian of the
+ * materialised probability map and GQA query / key gradients are reduced back
+ * to the KV heads).  For the scalar L = sum(O * dout) + sum(P * dprobs) with
+ * (O, P) the forward of (q, k, v), per (b, h, i), hk = h / (Hq / Hkv):
+ *     dP[i,j]  = sum_e dout[b,h,i,e] * v[b,hk,j,e] + dprobs[b,h,i,j]
+ *     rsum[i]  = sum_j P[i,j] * dP[i,j]
+ *     dS[i,j]  = P[i,j] * (dP[i,j] - rsum[i])        (softmax Jacobian)
+ *     dq[b,h,i,:]   = scale * sum_j dS[i,j] * k[b,hk,j,:]
+ *     dk[b,hk,j,:] += scale * dS[i,j] * q[b,h,i,:]    (summed over the group's heads)
+ *     dv[b,hk,j,:] += P[i,j] * dout[b,h,i,:]          (summed over the group's heads)
+ * Masked keys and fully masked rows have P = 0 and so no gradient; the mask
+ * itself gets none.  All double precision; P is taken as given (the forward's).
+ *
+ *   q [B,Hq,Sq,D], k [B,Hkv,Skv,D], v [B,Hkv,Skv,Dv], probs [B,Hq,Sq,Skv],
+ *   dout [B,Hq,Sq,Dv], dprobs [B,Hq,Sq,Skv] or NULL (no gradient through P);
+ *   outputs dq [B,Hq,Sq,D], dk [B,Hkv,Skv,D], dv [B,Hkv,Skv,Dv] (overwritten).
+ * Work is split over (b, hk): each owns its dk / dv rows, so the result does
+ * not depend on the thread count.
+ */
+int sdpa_oracle_bwd(const double *q, const double *k, const double *v,
+                    const double *probs, const double *dout, const double *dprobs,
+                    int64_t B, int64_t Hq, int64_t Hkv, int64_t Sq, int64_t Skv,
+                    int64_t D, int64_t Dv, double scale, double *dq, double *dk,
+                    double *dv, int nthreads) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || Sq < 0 || Skv < 0 || D < 0 || Dv < 0)
+        return ORACLE_ERR_ARGUMENT;
+    if (Hq % Hkv != 0) return ORACLE_ERR_ARGUMENT;
+    const int64_t g = Hq / Hkv;
+    if (nthreads < 1) nthreads = 1;
+    int failed = 0;
+#ifdef _OPENMP
+#pragma omp parallel num_threads(nthreads)
+#endif
+    {
+        double *dp = (double *)malloc((size_t)(Skv > 0 ? Skv : 1) * sizeof(double));
+        if (dp == NULL) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            failed = 1;
+        }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t bk = 0; bk < B * Hkv; ++bk) {
+            if (dp == NULL) continue;
+            const int64_t b = bk / Hkv, hk = bk % Hkv;
+            const double *kb = k + (b * Hkv + hk) * Skv * D;
+            const double *vb = v + (b * Hkv + hk) * Skv * Dv;
+            double *dkb = dk + (b * Hkv + hk) * Skv * D;
+            double *dvb = dv + (b * Hkv + hk) * Skv * Dv;
+            for (int64_t x = 0; x < Skv * D; ++x) dkb[x] = 0.0;
+            for (int64_t x = 0; x < Skv * Dv; ++x) dvb[x] = 0.0;
+            for (int64_t h = hk * g; h < (hk + 1) * g; ++h) {
+                for (int64_t i = 0; i < Sq; ++i) {
+                    const int64_t row = (b * Hq + h) * Sq + i;
+                    const double *pr = probs + row * Skv;
+                    const double *go = dout + row * Dv;
+                    const double *qr = q + row * D;
+                    double rsum = 0.0;
+                    for (int64_t j = 0; j < Skv; ++j) {
+                        double acc = dprobs ? dprobs[row * Skv + j] : 0.0;
+                        for (int64_t e = 0; e < Dv; ++e) acc += go[e] * vb[j * Dv + e];
+                        dp[j] = acc;
+                        rsum += pr[j] * acc;
+                    }
+                    double *dqr = dq + row * D;
+                    for (int64_t d = 0; d < D; ++d) dqr[d] = 0.0;
+                    for (int64_t j = 0; j < Skv; ++j) {
+                        const double ds = pr[j] * (dp[j] - rsum);
+                        for (int64_t d = 0; d < D; ++d) {
+                            dqr[d] += scale * ds * kb[j * D + d];
+                            dkb[j * D + d] += scale * ds * qr[d];
+                        }
+                        for (int64_t e = 0; e < Dv; ++e) dvb[j * Dv + e] += pr[j] * go[e];
+                    }
+                }
+            }
+        }
+        free(dp);
     }
     return failed ? ORACLE_ERR_ARGUMENT : ORACLE_OK;
 }
