@@ -175,6 +175,35 @@ sdpa_status sdpa_math_plan(const sdpa_tensor *q, const sdpa_tensor *k, const sdp
 sdpa_status sdpa_math_device_status(sdpa_stream_t stream);
 
 /*
+ * sdpa_math_bwd -- gradients of the (O, P) forward for q, k and v when both
+ * outputs carry a gradient (FlagOS-OP PR #10: the overview's A1 item, where
+ * the gradient flows through dout and dprobs; "2026-10-07 update: P800 fused
+ * backward", where dprobs goes through the exact softmax Jacobian of the
+ * materialised map and GQA gradients are reduced back to the KV heads):
+ *     dP = dout V^T + dprobs,   dS = P * (dP - rowsum(P * dP))
+ *     dq = scale dS K,   dk = scale dS^T Q,   dv = P^T dout
+ * with dk and dv summed over the query heads of each KV head.
+ *
+ *   q, k, v  the forward's inputs ([B,Hq,Sq,D], [B,Hkv,Skv,D], [B,Hkv,Skv,Dv]);
+ *   probs    the forward's P [B,Hq,Sq,Skv] (it already holds the mask and the
+ *            causal zeros, so neither is passed again; masked keys and fully
+ *            masked rows get no gradient);
+ *   dout     [B,Hq,Sq,Dv]; dprobs [B,Hq,Sq,Skv], or NULL for no gradient
+ *            through P;
+ *   dq, dk, dv  outputs with the shapes of q, k, v, fully overwritten;
+ *   rowsum   caller-owned DEVICE buffer of B*Hq*Sq floats, written with
+ *            rowsum(P * dP) per row ([B, Hq, Sq] order); the library
+ *            allocates nothing.
+ * All tensors share one dtype (f32 / f16 / bf16, fp32 accumulation), device
+ * pointers, unit innermost stride; D, Dv <= 256.  Asynchronous on `stream`.
+ * Errors as sdpa_math_fwd (argument checks on the host before any launch).
+ */
+sdpa_status sdpa_math_bwd(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
+                          const sdpa_tensor *probs, const sdpa_tensor *dout, const sdpa_tensor *dprobs,
+                          float scale, sdpa_tensor *dq, sdpa_tensor *dk, sdpa_tensor *dv, float *rowsum,
+                          sdpa_stream_t stream);
+
+/*
  * sdpa_math_selftest_wait -- diagnostic for the failure path above.  Enqueues
  * on `stream` one single-thread kernel that waits, through the same bounded
  * mbarrier wait the tensor-core kernels use, on a barrier nothing ever

@@ -41,6 +41,25 @@ inline int64_t live_tiles_per_slice(int64_t Sq, int64_t Skv, bool causal) {
     return n;
 }
 
+// The backward's validated arguments (element strides for [B, H, S] of every
+// tensor; the innermost stride is 1).  dprobs may be null (no gradient through
+// P); rowsum is the caller's B*Hq*Sq float buffer for sum_j P dP per row.
+struct BwdProblem {
+    int dtype;
+    int64_t B, Hq, Hkv, Sq, Skv, D, Dv, group;
+    const void* q;  int64_t sq[3];
+    const void* k;  int64_t sk[3];
+    const void* v;  int64_t sv[3];
+    const void* p;  int64_t sp[3];
+    const void* dout; int64_t sgo[3];
+    const void* dprobs; int64_t sgp[3];
+    void* dq; int64_t sdq[3];
+    void* dk; int64_t sdk[3];
+    void* dv; int64_t sdv[3];
+    float* rowsum;
+    float scale;
+};
+
 // Kernel launchers.  Each returns cudaSuccess or the launch error.  `why`
 // receives a static reason string when a launcher cannot serve the problem
 // (then it returns cudaErrorNotSupported without launching).
@@ -53,6 +72,7 @@ cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream);
 int tc_query_tiles(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdProblem& p, cudaStream_t stream);
 
 // Device error word shared by every kernel of the library (see
 // sdpa_math_device_status).  read_and_clear returns the word's old value.

@@ -315,6 +315,64 @@ sdpa_status sdpa_math_device_status(sdpa_stream_t stream) {
     return SDPA_OK;
 }
 
+sdpa_status sdpa_math_bwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                          const sdpa_tensor* probs, const sdpa_tensor* dout, const sdpa_tensor* dprobs,
+                          float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv, float* rowsum,
+                          sdpa_stream_t stream) {
+    g_last_error.clear();
+    sdpa_status s;
+    const sdpa_tensor* all[] = {q, k, v, probs, dout, dq, dk, dv};
+    const char* names[] = {"q", "k", "v", "probs", "dout", "dq", "dk", "dv"};
+    for (int i = 0; i < 8; ++i)
+        if ((s = check_tensor(all[i], names[i])) != SDPA_OK) return s;
+    if (dprobs && (s = check_tensor(dprobs, "dprobs")) != SDPA_OK) return s;
+    if (q->dtype != SDPA_F32 && q->dtype != SDPA_F16 && q->dtype != SDPA_BF16)
+        return fail(SDPA_ERR_UNSUPPORTED, "q: dtype %s is not f32/f16/bf16", dtype_name(q->dtype));
+    for (int i = 1; i < 8; ++i)
+        if (all[i]->dtype != q->dtype)
+            return fail(SDPA_ERR_INVALID_ARGUMENT, "%s: dtype %s differs from q dtype %s", names[i],
+                        dtype_name(all[i]->dtype), dtype_name(q->dtype));
+    if (dprobs && dprobs->dtype != q->dtype)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "dprobs: dtype differs from q");
+    const int64_t B = q->shape[0], Hq = q->shape[1], Sq = q->shape[2], D = q->shape[3];
+    const int64_t Hkv = k->shape[1], Skv = k->shape[2], Dv = v->shape[3];
+    if (k->shape[0] != B || !same_shape(v, B, Hkv, Skv, Dv) || k->shape[3] != D)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "k must be [B,Hkv,Skv,D] and v [B,Hkv,Skv,Dv] for q [B,Hq,Sq,D]");
+    if (Hkv <= 0 ? Hq != 0 : (Hq % Hkv) != 0)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "GQA requires Hq divisible by Hkv (Hq=%lld, Hkv=%lld)",
+                    (long long)Hq, (long long)Hkv);
+    if (D > 256 || Dv > 256) return fail(SDPA_ERR_UNSUPPORTED, "head dim above 256 is not supported");
+    if (!std::isfinite(scale)) return fail(SDPA_ERR_INVALID_ARGUMENT, "scale must be finite");
+    if (!same_shape(probs, B, Hq, Sq, Skv) || (dprobs && !same_shape(dprobs, B, Hq, Sq, Skv)))
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "probs and dprobs must be [B,Hq,Sq,Skv]");
+    if (!same_shape(dout, B, Hq, Sq, Dv)) return fail(SDPA_ERR_INVALID_ARGUMENT, "dout must be [B,Hq,Sq,Dv]");
+    if (!same_shape(dq, B, Hq, Sq, D) || !same_shape(dk, B, Hkv, Skv, D) || !same_shape(dv, B, Hkv, Skv, Dv))
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "dq, dk, dv must have the shapes of q, k, v");
+    if (B * Hq * Sq > 0 && (!rowsum || ((uintptr_t)rowsum) % 4 != 0))
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "rowsum must be a 4-byte aligned device buffer of B*Hq*Sq floats");
+    sdpa::BwdProblem p;
+    std::memset(&p, 0, sizeof(p));
+    p.dtype = q->dtype;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Sq = Sq; p.Skv = Skv; p.D = D; p.Dv = Dv;
+    p.group = Hkv > 0 ? Hq / Hkv : 1;
+    auto set = [](const sdpa_tensor* t, const void** ptr, int64_t* st) {
+        *ptr = t ? t->data : nullptr;
+        for (int i = 0; i < 3; ++i) st[i] = t ? t->stride[i] : 0;
+    };
+    set(q, &p.q, p.sq); set(k, &p.k, p.sk); set(v, &p.v, p.sv); set(probs, &p.p, p.sp);
+    set(dout, &p.dout, p.sgo); set(dprobs, &p.dprobs, p.sgp);
+    const void* tmp;
+    set(dq, &tmp, p.sdq); p.dq = dq->data;
+    set(dk, &tmp, p.sdk); p.dk = dk->data;
+    set(dv, &tmp, p.sdv); p.dv = dv->data;
+    p.rowsum = rowsum;
+    p.scale = scale;
+    if (B * Hkv == 0 || (Sq == 0 && Skv == 0)) return SDPA_OK;
+    const cudaError_t e = sdpa::launch_bwd(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    return SDPA_OK;
+}
+
 sdpa_status sdpa_math_selftest_wait(sdpa_stream_t stream) {
     g_last_error.clear();
     const cudaError_t e = sdpa::launch_selftest_wait(reinterpret_cast<cudaStream_t>(stream));

@@ -222,3 +222,34 @@ def test_fused_needs_at_most_256_keys(lib):
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "fused"
     q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=264, D=64)
     _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant="fused"), "256 keys")
+
+
+def _bwd_args(B=1, Hq=4, Hkv=2, Sq=9, Skv=11, D=16, Dv=8, dtype=torch.float16):
+    q = torch.zeros(B, Hq, Sq, D, dtype=dtype)
+    k = torch.zeros(B, Hkv, Skv, D, dtype=dtype)
+    v = torch.zeros(B, Hkv, Skv, Dv, dtype=dtype)
+    P = torch.zeros(B, Hq, Sq, Skv, dtype=dtype)
+    go = torch.zeros(B, Hq, Sq, Dv, dtype=dtype)
+    return q, k, v, P, go, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+
+def test_backward_argument_errors(lib):
+    """Host-side checks of sdpa_math_bwd (they return before any launch; the
+    stream handle is never used on these paths)."""
+    q, k, v, P, go, dq, dk, dv = _bwd_args()
+    rs = torch.zeros(1, 4, 9)
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P[..., :10], go, None, 0.25, dq, dk, dv, rs, stream=0), "probs")
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P, go[..., :7], None, 0.25, dq, dk, dv, rs, stream=0), "dout")
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P, go, None, 0.25, dq, dk[:, :1], dv, rs, stream=0), "dq, dk, dv")
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P, go, None, 0.25, dq, dk, dv, None, stream=0), "rowsum")
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P.float(), go, None, 0.25, dq, dk, dv, rs, stream=0), "dtype")
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P, go, P[..., :3], 0.25, dq, dk, dv, rs, stream=0), "dprobs")
+    q6, k6, v6, P6, go6, dq6, dk6, dv6 = _bwd_args(Hq=6, Hkv=4)
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q6, k6, v6, P6, go6, None, 0.25, dq6, dk6, dv6, rs, stream=0), "divisible")
