@@ -225,10 +225,37 @@ def oracle_sample_ms(w: W.Workload, budget_s: float, inputs=None):
     return ms, threads, sample
 
 
+def run_reference_bwd(args, w: W.Workload):
+    """The oracle backward (on one (batch, KV head) group, extrapolated), as the
+    reference arm of --pass bwd."""
+    import oracle
+    q, k, v, m = W.make_inputs(w)
+    _, Po, _ = oracle.oracle_fwd(q, k, v, m, is_causal=w.is_causal, scale=w.scale,
+                                 nthreads=max(1, os.cpu_count() or 1))
+    P = torch.from_numpy(Po).to(w.torch_dtype)
+    g = torch.Generator().manual_seed(w.seed + 100)
+    go = torch.randn(w.B, w.Hq, w.Sq, w.D, generator=g).to(w.torch_dtype)
+    gp = torch.randn(P.shape, generator=g).to(w.torch_dtype)
+    vals = [oracle_bwd_sample_ms(w, q, k, v, P, go, gp) for _ in range(max(1, args.steps))]
+    ms = statistics.mean(x[0] for x in vals)
+    line = {
+        "impl": "reference", "metric": METRIC_BWD, "value": ms, "unit": "ms", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "pass": "bwd"},
+        "cpu_baseline": {"value": ms, "unit": "ms", "cores": 1, "kind": "oracle", "sample": vals[0][2]},
+        "e2e": {"value": ms, "unit": "ms", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_reference(args, w: W.Workload):
     world, rank, _ = dist_setup("gloo")
     if rank != 0:
         return 0
+    if args.pass_ == "bwd":
+        return run_reference_bwd(args, w)
     inputs = W.make_inputs(w)
     per_step = max(0.05, min(args.cpu_budget, 10.0, 150.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
@@ -382,6 +409,153 @@ def run_ours(args, w: W.Workload):
     return 0
 
 
+# ----------------------------------------------------------------------------- backward
+
+METRIC_BWD = "(dq,dk,dv) bwd ms and HBM GB/s; % of roofline (1×GB300)"
+
+
+def bwd_bytes(w: W.Workload) -> int:
+    """Algorithmic bytes of the backward: q, k, v, P, dout, dprobs read once;
+    dq, dk, dv and the fp32 per-row sums written once."""
+    e = 4 if w.dtype == "f32" else 2
+    rows = w.B * w.Hq * w.Sq
+    # D == Dv for every workload: q, dout, dq rows; k, v, dk, dv rows; P and dprobs
+    return e * (3 * rows * w.D + 4 * w.B * w.Hkv * w.Skv * w.D + 2 * rows * w.Skv) + 4 * rows
+
+
+def oracle_bwd_sample_ms(w: W.Workload, q, k, v, P, go, gp):
+    """The oracle backward on one (batch, KV head) group, extrapolated to all
+    B * Hkv groups (groups are independent and equal in size)."""
+    import oracle
+    g = w.Hq // w.Hkv
+    sl = lambda t, H: t[:1, :H].contiguous()
+    qs, ks, vs = sl(q, g), sl(k, 1), sl(v, 1)
+    Ps, gos, gps = sl(P, g), sl(go, g), sl(gp, g)
+    threads = max(1, os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    oracle.oracle_bwd(qs, ks, vs, Ps, gos, gps, scale=w.scale, nthreads=threads)
+    dt = time.perf_counter() - t0
+    groups = w.B * w.Hkv
+    sample = (f"1 of {groups} (batch, KV head) groups ({g} query heads x {w.Sq} rows x {w.Skv} keys), "
+              f"fp64 C oracle backward, {dt:.2f} s, extrapolated to all groups (one thread per group)")
+    return dt * 1e3 * groups, 1, sample
+
+
+def run_ours_bwd(args, w: W.Workload):
+    import sdpa_forward_materialised_gb300 as sm
+    world, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sm.load_library()
+    q, k, v, m = W.make_inputs(w)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    md = m.to(dev) if m is not None else None
+    O, P = sm.sdpa_math(qd, kd, vd, md, is_causal=w.is_causal, scale=w.scale)  # the forward's map
+    g = torch.Generator().manual_seed(w.seed + 100)
+    go = torch.randn(O.shape, generator=g).to(w.torch_dtype)
+    gp = torch.randn(P.shape, generator=g).to(w.torch_dtype)
+    god, gpd = go.to(dev), gp.to(dev)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    rowsum = torch.empty(qd.shape[:3], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_rd = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.sum()
+        torch.cuda._sleep(200_000)
+
+    def step():
+        sm.sdpa_math_bwd(qd, kd, vd, P, god, gpd, w.scale, dq, dk, dv, rowsum, stream)
+
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize(dev)
+    sm.sdpa_math_device_status(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush_l2()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t1 = time.perf_counter()
+    time.sleep(0.15)
+    sampler.stop()
+    sm.sdpa_math_device_status(stream)
+    ms = max_over_ranks(statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends)), world, dev)
+    clocks = sampler.summary(t0, t1)
+
+    # end to end: inputs from pinned host memory, gradients back to it
+    hosts = [t.pin_memory() for t in (q, k, v, P.cpu(), go, gp)]
+    devs = [qd, kd, vd, P, god, gpd]
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in hosts)
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    e2e_steps = max(3, min(args.steps, 50))
+
+    def e2e_step():
+        for d, h in zip(devs, hosts):
+            d.copy_(h, non_blocking=True)
+        step()
+        for o, d in zip(outs, (dq, dk, dv)):
+            o.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    es.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ee.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(es.elapsed_time(ee) / e2e_steps, world, dev)
+
+    peaks, peak_src = load_peaks()
+    nbytes = bwd_bytes(w)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    hbm_peak = float(peaks["hbm_gbs"])
+    line = {
+        "metric": METRIC_BWD, "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "pass": "bwd", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
+                   "Skv": w.Skv, "D": w.D, "is_causal": w.is_causal, "mask": w.mask, "seed": w.seed,
+                   "kernels": "CUDA-core rows + keys kernels",
+                   "l2": "flushed before every step (256 MiB write, then 256 MiB read)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "hbm_gbs": gbs, "algorithmic_bytes": nbytes,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} (copy bandwidth, burst)"},
+        "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 2,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cms, threads, sample = oracle_bwd_sample_ms(w, q, k, v, P.cpu(), go, gp)
+        line["cpu_baseline"] = {"value": cms, "unit": "ms", "cores": threads, "kind": "oracle",
+                                "sample": sample}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def ncu_traffic(w: W.Workload, variant: str):
     """DRAM bytes per launch from the committed ncu summary, only when it was
     taken on the kernel sources as they are now (else None)."""
@@ -411,11 +585,15 @@ def main(argv=None):
     ap.add_argument("--variant", default="auto", choices=["auto", "simt", "twopass", "paired", "fused", "decode"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                    help="fwd: the (O, P) forward (the headline); bwd: the backward for dout and dprobs")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)  # at least three untimed warm-up steps
     w = W.BY_NAME[args.config]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.pass_ == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 
