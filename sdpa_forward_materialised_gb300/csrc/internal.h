@@ -72,6 +72,8 @@ cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream);
 int tc_query_tiles(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
+bool split_supports(const Problem& p, const char** why);
+cudaError_t launch_split(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdProblem& p, cudaStream_t stream);
 
 // Device error word shared by every kernel of the library (see

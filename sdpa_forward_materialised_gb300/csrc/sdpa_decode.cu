@@ -104,6 +104,8 @@ struct DecParams {
     int off_v, off_q, off_s, off_o, off_stat;  // shared-memory layout (bytes)
 };
 
+__device__ __forceinline__ void cp_async_wait_ring() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
 // RM is a compile-time bound on the query rows (R <= RM), so the per-row
 // accumulators of the score phase stay in registers.
 template <typename T, int RM>
@@ -338,6 +340,286 @@ decode_kernel(const DecParams p) {
     cluster_sync();  // no CTA leaves while a peer may still read its shared memory
 }
 
+
+// ---------------------------------------------------------------------------
+// Split-KV kernel for long key sequences (few query rows, many keys).
+//
+// The same cluster decomposition as decode_kernel (one cluster of C CTAs per
+// (batch, key/value head), CTA c owns a contiguous chunk of keys, statistics
+// and partial O combined through distributed shared memory), with the parts
+// that tie decode_kernel to short chunks taken out:
+//   * a thread walks its keys t, t + 256, ... of the chunk, K rows read
+//     straight into registers with the next 128-byte batch in flight while the
+//     current one is used; the scores of the whole chunk stay in shared memory;
+//   * V is not staged whole: 64-key sub-tiles stream through a two-slot ring of
+//     asynchronous copies (the first two are issued before the score phase);
+//   * P V: a thread owns (key group, pair of O columns) and accumulates all R
+//     rows, so every V element is read from shared memory once per CTA;
+//   * clusters of up to 16 CTAs (non-portable size, 8 where 16 cannot be
+//     scheduled).
+// ---------------------------------------------------------------------------
+constexpr int kSplitMaxCluster = 16;
+constexpr int kSplitTK = 64;                 // keys per V sub-tile
+constexpr int kSplitSmemBudget = 220 * 1024;
+
+template <typename T, int RM>
+__global__ void __launch_bounds__(kThreads, RM <= 8 ? 2 : 1)
+split_kernel(const DecParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float lse_s[kMaxRows];
+    __shared__ int row_h[kMaxRows], row_i[kMaxRows];
+
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    const uint32_t crank = cluster_rank();
+    const int C = (int)(gridDim.x);
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int k0 = (int)crank * p.chunk;
+    const int n = max(0, min(p.Skv, k0 + p.chunk) - k0);
+    const int R = p.rows, D = p.D, Dv = p.Dv;
+    constexpr int es = (int)sizeof(T);
+
+    uint8_t* vr = smem + p.off_v;                             // [2][kSplitTK][Dv] V ring (dtype)
+    float* qs = reinterpret_cast<float*>(smem + p.off_q);     // [R][D] query rows (fp32)
+    float* ss = reinterpret_cast<float*>(smem + p.off_s);     // [R][chunk] scores, then rounded P
+    float* part = reinterpret_cast<float*>(smem + p.off_o);   // [G][R][Dv] partial O per key group
+    float* st = reinterpret_cast<float*>(smem + p.off_stat);  // [R][2] chunk (max, sum)
+
+    const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
+    const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
+    const int uv = Dv * es / 16;  // 16-byte units per V row
+    const int ntile = (n + kSplitTK - 1) / kSplitTK;
+    auto issue_v = [&](int tile) {  // one commit group per call (empty past the last tile)
+        if (tile < ntile) {
+            const int j0 = tile * kSplitTK, len = min(kSplitTK, n - j0);
+            uint8_t* dst = vr + (tile & 1) * kSplitTK * Dv * es;
+            for (int u = t; u < len * uv; u += kThreads) {
+                const int r = u / uv, c = u % uv;
+                cp_async16(dst + 16 * u, reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * c);
+            }
+        }
+        cp_async_commit();
+    };
+
+    // ---- 1. query rows (fp32) and the first two V sub-tiles
+    for (int e = t; e < R * D; e += kThreads) {
+        const int r = e / D, d = e % D;
+        const T* qr = static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
+                      (long long)(r % p.Sq) * p.sq2;
+        qs[e] = to_f(qr[d]);
+    }
+    if (t < R) {
+        row_h[t] = hk * p.group + t / p.Sq;
+        row_i[t] = t % p.Sq;
+    }
+    issue_v(0);
+    issue_v(1);
+    __syncthreads();
+
+    // ---- 2. scores of this thread's keys; unit u = (key t + 256 * (u / nb),
+    // bytes [128 * (u % nb), +128) of its K row)
+    {
+        const int kbytes = D * es;
+        const int nb = (kbytes + 127) / 128;
+        const int nk = t < n ? (n - t + kThreads - 1) / kThreads : 0;
+        const int nu = nk * nb;
+        const uint8_t* kbase = reinterpret_cast<const uint8_t*>(K);
+        uint4 cur[8], nxt[8];
+        auto load_unit = [&](int u, uint4 (&dst)[8]) {
+            const int key = t + kThreads * (u / nb), b0 = 128 * (u % nb);
+            const uint8_t* src = kbase + ((long long)key * p.sk2) * es + b0;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                if (b0 + 16 * x < kbytes) dst[x] = __ldg(reinterpret_cast<const uint4*>(src + 16 * x));
+        };
+        if (nu > 0) load_unit(0, cur);
+        float acc[RM];
+#pragma unroll
+        for (int r = 0; r < RM; ++r) acc[r] = 0.f;
+        for (int u = 0; u < nu; ++u) {
+            if (u + 1 < nu) load_unit(u + 1, nxt);
+            const int b0 = 128 * (u % nb);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                if (b0 + 16 * x >= kbytes) break;
+                const int d = (b0 + 16 * x) / es;
+                if constexpr (es == 4) {
+                    const float4 kk = make_float4(__uint_as_float(cur[x].x), __uint_as_float(cur[x].y),
+                                                  __uint_as_float(cur[x].z), __uint_as_float(cur[x].w));
+#pragma unroll
+                    for (int r = 0; r < RM; ++r)
+                        if (r < R) {
+                            const float4 qq = *reinterpret_cast<const float4*>(&qs[r * D + d]);
+                            float a = acc[r];
+                            a = fmaf(qq.x, kk.x, a);
+                            a = fmaf(qq.y, kk.y, a);
+                            a = fmaf(qq.z, kk.z, a);
+                            a = fmaf(qq.w, kk.w, a);
+                            acc[r] = a;
+                        }
+                } else {
+                    const float2 k01 = unpack2<T>(cur[x].x), k23 = unpack2<T>(cur[x].y);
+                    const float2 k45 = unpack2<T>(cur[x].z), k67 = unpack2<T>(cur[x].w);
+#pragma unroll
+                    for (int r = 0; r < RM; ++r)
+                        if (r < R) {
+                            const float4 qa = *reinterpret_cast<const float4*>(&qs[r * D + d]);
+                            const float4 qb = *reinterpret_cast<const float4*>(&qs[r * D + d + 4]);
+                            float a = acc[r];
+                            a = fmaf(qa.x, k01.x, a);
+                            a = fmaf(qa.y, k01.y, a);
+                            a = fmaf(qa.z, k23.x, a);
+                            a = fmaf(qa.w, k23.y, a);
+                            a = fmaf(qb.x, k45.x, a);
+                            a = fmaf(qb.y, k45.y, a);
+                            a = fmaf(qb.z, k67.x, a);
+                            a = fmaf(qb.w, k67.y, a);
+                            acc[r] = a;
+                        }
+                }
+            }
+            if (u % nb == nb - 1) {  // this key's dot products are complete
+                const int j = t + kThreads * (u / nb), key = k0 + j;
+#pragma unroll
+                for (int r = 0; r < RM; ++r)
+                    if (r < R) {
+                        float s = __fmul_rn(acc[r], p.c2);
+                        if (p.causal && key > row_i[r]) s = -CUDART_INF_F;
+                        if (p.mask_kind != kMaskNone) {
+                            const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + key;
+                            if (p.mask_kind == kMaskBool) {
+                                if (static_cast<const unsigned char*>(p.mask)[off] == 0) s = -CUDART_INF_F;
+                            } else {
+                                const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                                     : to_f(static_cast<const T*>(p.mask)[off]);
+                                s = __fmaf_rn(m, kLog2e, s);
+                            }
+                        }
+                        ss[r * p.chunk + j] = s;
+                        acc[r] = 0.f;
+                    }
+            }
+#pragma unroll
+            for (int x = 0; x < 8; ++x) cur[x] = nxt[x];
+        }
+    }
+    __syncthreads();
+
+    // per-row (max, sum of exp2) of the chunk: one warp per row
+    for (int r = warp; r < R; r += kThreads / 32) {
+        float m = -CUDART_INF_F;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, ss[r * p.chunk + j]);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        if (m != -CUDART_INF_F)
+            for (int j = lane; j < n; j += 32) l += exp2f(ss[r * p.chunk + j] - m);
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            st[2 * r] = m;
+            st[2 * r + 1] = l;
+        }
+    }
+
+    // ---- 3. the cluster's statistics -> the same lse in every CTA
+    cluster_sync();
+    if (t < R) {
+        float mc[kSplitMaxCluster], lc[kSplitMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kSplitMaxCluster; ++c)
+            if (c < C) {
+                mc[c] = ld_peer(peer_addr(&st[2 * t], (uint32_t)c));
+                lc[c] = ld_peer(peer_addr(&st[2 * t + 1], (uint32_t)c));
+            }
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < kSplitMaxCluster; ++c)
+            if (c < C) m = fmaxf(m, mc[c]);
+        float l = 0.f;
+        if (m != -CUDART_INF_F) {
+#pragma unroll
+            for (int c = 0; c < kSplitMaxCluster; ++c)
+                if (c < C && mc[c] != -CUDART_INF_F) l += lc[c] * exp2f(mc[c] - m);
+        }
+        lse_s[t] = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
+    }
+    __syncthreads();
+
+    // ---- 4. per V sub-tile: P (stored, kept rounded), then P V
+    const int DP = Dv / 2;                // column pairs (Dv is even)
+    const int G = kThreads / DP;          // key groups
+    const int kg = t / DP, dp = 2 * (t % DP);
+    float a0[RM], a1[RM];
+#pragma unroll
+    for (int r = 0; r < RM; ++r) a0[r] = a1[r] = 0.f;
+    for (int tile = 0; tile < ntile; ++tile) {
+        const int j0 = tile * kSplitTK, len = min(kSplitTK, n - j0);
+        for (int e = t; e < R * len; e += kThreads) {
+            const int r = e / len, j = j0 + e % len;
+            const float L = lse_s[r];
+            const float pr = (L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L);
+            const T pt = from_f<T>(pr);
+            T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
+            prow[k0 + j] = pt;
+            ss[r * p.chunk + j] = to_f(pt);
+        }
+        cp_async_wait_ring();  // this sub-tile's group is complete (at most the next one is pending)
+        __syncthreads();
+        if (kg < G) {
+            const uint8_t* vt = vr + (tile & 1) * kSplitTK * Dv * es;
+            for (int jj = kg; jj < len; jj += G) {
+                float2 vv;
+                if constexpr (es == 4) vv = *reinterpret_cast<const float2*>(vt + (jj * Dv + dp) * 4);
+                else vv = unpack2<T>(*reinterpret_cast<const uint32_t*>(vt + (jj * Dv + dp) * 2));
+                const float* pc = ss + j0 + jj;
+#pragma unroll
+                for (int r = 0; r < RM; ++r)
+                    if (r < R) {
+                        const float pv = pc[r * p.chunk];
+                        a0[r] = fmaf(pv, vv.x, a0[r]);
+                        a1[r] = fmaf(pv, vv.y, a1[r]);
+                    }
+            }
+        }
+        __syncthreads();   // every thread is done with this ring slot
+        issue_v(tile + 2);
+    }
+    cp_async_wait_all();
+    if (kg < G) {
+#pragma unroll
+        for (int r = 0; r < RM; ++r)
+            if (r < R) *reinterpret_cast<float2*>(&part[(kg * R + r) * Dv + dp]) = make_float2(a0[r], a1[r]);
+    }
+    __syncthreads();
+    for (int e = t; e < R * Dv; e += kThreads) {  // sum of the key groups, in place in group 0
+        float s = 0.f;
+        for (int g = 0; g < G; ++g) s += part[g * R * Dv + e];
+        part[e] = s;
+    }
+
+    // ---- 5. sum this CTA's slice of the O columns over the cluster
+    cluster_sync();
+    const int cols = (Dv + C - 1) / C;
+    const int c0 = (int)crank * cols, c1 = min(Dv, c0 + cols);
+    for (int e = t; e < R * max(0, c1 - c0); e += kThreads) {
+        const int r = e / (c1 - c0), d = c0 + e % (c1 - c0);
+        float pc[kSplitMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kSplitMaxCluster; ++c)
+            if (c < C) pc[c] = ld_peer(peer_addr(&part[r * Dv + d], (uint32_t)c));
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kSplitMaxCluster; ++c)
+            if (c < C) acc += pc[c];
+        const bool dead = lse_s[r] == -CUDART_INF_F;
+        T* orow = static_cast<T*>(p.o) + b * p.so0 + row_h[r] * p.so1 + (long long)row_i[r] * p.so2;
+        orow[d] = from_f<T>(dead ? 0.f : acc);
+    }
+    if (crank == 0 && p.lse && t < R) {
+        const float L = lse_s[t];
+        p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
+    }
+    cluster_sync();
+}
+
 int elem_bytes(int dt) { return dt == kF32 ? 4 : 2; }
 
 // Cluster size and chunk for a problem, and the shared-memory bytes it needs.
@@ -363,23 +645,28 @@ struct Ready { const void* kern; int dev; };
 Ready g_ready[32];
 int g_nready = 0;
 
+void fill_params(const Problem& pr, DecParams* p) {
+    p->q = pr.q; p->sq0 = pr.sq[0]; p->sq1 = pr.sq[1]; p->sq2 = pr.sq[2];
+    p->k = pr.k; p->sk0 = pr.sk[0]; p->sk1 = pr.sk[1]; p->sk2 = pr.sk[2];
+    p->v = pr.v; p->sv0 = pr.sv[0]; p->sv1 = pr.sv[1]; p->sv2 = pr.sv[2];
+    p->mask = pr.mask; p->mask_kind = pr.mask_kind; p->mask_dtype = pr.mask_dtype;
+    p->sm0 = pr.sm[0]; p->sm1 = pr.sm[1]; p->sm2 = pr.sm[2];
+    p->o = pr.o; p->so0 = pr.so[0]; p->so1 = pr.so[1]; p->so2 = pr.so[2];
+    p->p = pr.p; p->sp0 = pr.sp[0]; p->sp1 = pr.sp[1]; p->sp2 = pr.sp[2];
+    p->lse = pr.lse;
+    p->Hq = (int)pr.Hq; p->Sq = (int)pr.Sq; p->Skv = (int)pr.Skv; p->D = (int)pr.D; p->Dv = (int)pr.Dv;
+    p->group = (int)pr.group; p->rows = (int)(pr.group * pr.Sq); p->causal = pr.causal;
+    p->c2 = pr.scale * kLog2e;
+}
+
 template <typename T, int RM>
 cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
     DecParams p;
     std::memset(&p, 0, sizeof(p));
     int C, chunk, smem;
     plan(pr, &C, &chunk, &p, &smem);
-    p.q = pr.q; p.sq0 = pr.sq[0]; p.sq1 = pr.sq[1]; p.sq2 = pr.sq[2];
-    p.k = pr.k; p.sk0 = pr.sk[0]; p.sk1 = pr.sk[1]; p.sk2 = pr.sk[2];
-    p.v = pr.v; p.sv0 = pr.sv[0]; p.sv1 = pr.sv[1]; p.sv2 = pr.sv[2];
-    p.mask = pr.mask; p.mask_kind = pr.mask_kind; p.mask_dtype = pr.mask_dtype;
-    p.sm0 = pr.sm[0]; p.sm1 = pr.sm[1]; p.sm2 = pr.sm[2];
-    p.o = pr.o; p.so0 = pr.so[0]; p.so1 = pr.so[1]; p.so2 = pr.so[2];
-    p.p = pr.p; p.sp0 = pr.sp[0]; p.sp1 = pr.sp[1]; p.sp2 = pr.sp[2];
-    p.lse = pr.lse;
-    p.Hq = (int)pr.Hq; p.Sq = (int)pr.Sq; p.Skv = (int)pr.Skv; p.D = (int)pr.D; p.Dv = (int)pr.Dv;
-    p.group = (int)pr.group; p.rows = (int)(pr.group * pr.Sq); p.chunk = chunk; p.causal = pr.causal;
-    p.c2 = pr.scale * kLog2e;
+    fill_params(pr, &p);
+    p.chunk = chunk;
 
     auto kern = decode_kernel<T, RM>;
     int dev = 0;
@@ -415,6 +702,106 @@ cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Shared-memory layout of split_kernel for a cluster of C CTAs; false when it
+// exceeds the budget.
+bool plan_split(const Problem& p, int C, int* chunk, DecParams* dp, int* smem) {
+    const long long ch = (p.Skv + C - 1) / C;
+    const long long rows = p.group * p.Sq, es = elem_bytes(p.dtype);
+    const long long G = kThreads / (p.Dv / 2);
+    long long off = 0;
+    auto al = [](long long x) { return (x + 15) & ~15ll; };
+    const long long off_v = off; off = al(off + 2ll * kSplitTK * p.Dv * es);
+    const long long off_q = off; off = al(off + rows * p.D * 4);
+    const long long off_s = off; off = al(off + rows * ch * 4);
+    const long long off_o = off; off = al(off + G * rows * p.Dv * 4);
+    const long long off_st = off; off += rows * 2 * 4;
+    if (off > kSplitSmemBudget) return false;
+    *chunk = (int)ch;
+    dp->off_v = (int)off_v; dp->off_q = (int)off_q; dp->off_s = (int)off_s; dp->off_o = (int)off_o;
+    dp->off_stat = (int)off_st;
+    *smem = (int)off;
+    return true;
+}
+
+// Cluster size per (kernel, device, shared memory): 16 where the GPU can
+// schedule such a cluster with that much shared memory per CTA, else 8.
+struct SplitChoice { const void* kern; int dev; int smem; int C; };
+SplitChoice g_split[64];
+int g_nsplit = 0;
+const void* g_split_attr_kern[64];
+int g_split_attr_dev[64];
+int g_nsplit_attr = 0;
+
+template <typename T, int RM>
+cudaError_t launch_split_rm(const Problem& pr, cudaStream_t stream) {
+    auto kern = split_kernel<T, RM>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    bool ready = false;
+    for (int i = 0; i < g_nsplit_attr; ++i)
+        ready |= g_split_attr_kern[i] == reinterpret_cast<const void*>(kern) && g_split_attr_dev[i] == dev;
+    if (!ready) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSplitSmemBudget);
+        if (e != cudaSuccess) return e;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            (void)cudaGetLastError();  // then only portable sizes are offered below
+        if (g_nsplit_attr < 64) {
+            g_split_attr_kern[g_nsplit_attr] = reinterpret_cast<const void*>(kern);
+            g_split_attr_dev[g_nsplit_attr++] = dev;
+        }
+    }
+    DecParams p;
+    std::memset(&p, 0, sizeof(p));
+    fill_params(pr, &p);
+    int chunk = 0, smem = 0, C = kSplitMaxCluster;
+    if (!plan_split(pr, C, &chunk, &p, &smem)) return cudaErrorNotSupported;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int chosen = 0;
+    for (int i = 0; i < g_nsplit; ++i)
+        if (g_split[i].kern == reinterpret_cast<const void*>(kern) && g_split[i].dev == dev && g_split[i].smem == smem)
+            chosen = g_split[i].C;
+    if (chosen == 0) {
+        int nc = 0;
+        cfg.gridDim = dim3((unsigned)kSplitMaxCluster, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        attr[0].val.clusterDim.x = (unsigned)kSplitMaxCluster;
+        if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();
+            nc = 0;
+        }
+        chosen = nc > 0 ? kSplitMaxCluster : kMaxCluster;
+        if (g_nsplit < 64) g_split[g_nsplit++] = SplitChoice{reinterpret_cast<const void*>(kern), dev, smem, chosen};
+    }
+    C = chosen;
+    if (C != kSplitMaxCluster && !plan_split(pr, C, &chunk, &p, &smem)) return cudaErrorNotSupported;
+    p.chunk = chunk;
+    cfg.gridDim = dim3((unsigned)C, (unsigned)pr.Hkv, (unsigned)pr.B);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_split_t(const Problem& p, cudaStream_t stream) {
+    const int64_t rows = p.group * p.Sq;
+    if (rows <= 4) return launch_split_rm<T, 4>(p, stream);
+    if (rows <= 8) return launch_split_rm<T, 8>(p, stream);
+    return launch_split_rm<T, 16>(p, stream);
+}
+
 template <typename T>
 cudaError_t launch_t(const Problem& p, cudaStream_t stream) {
     const int64_t rows = p.group * p.Sq;
@@ -443,6 +830,37 @@ bool decode_supports(const Problem& p, const char** why) {
     if (chunk > kThreads) { *why = "more than 2048 keys (one thread per key of a chunk)"; return false; }
     if (smem > kSmemBudget) { *why = "key chunk too long for shared memory"; return false; }
     return true;
+}
+
+bool split_supports(const Problem& p, const char** why) {
+    if (p.group * p.Sq > kMaxRows) { *why = "more than 16 query rows per key/value head"; return false; }
+    if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
+    if (p.D > 256 || p.Dv > 256) { *why = "head dim above 256"; return false; }
+    if (p.B > 65535 || p.Hkv > 65535 || p.Skv >= (1ll << 31)) { *why = "sizes beyond the grid limits"; return false; }
+    const int es = elem_bytes(p.dtype);
+    if ((p.D * es) % 16 != 0 || (p.Dv * es) % 16 != 0) { *why = "head dims must be 16-byte multiples"; return false; }
+    if (!aligned16(p.k) || !aligned16(p.v) || (p.sk[2] * es) % 16 != 0 || (p.sv[2] * es) % 16 != 0 ||
+        (p.Hkv > 1 && ((p.sk[1] * es) % 16 != 0 || (p.sv[1] * es) % 16 != 0)) ||
+        (p.B > 1 && ((p.sk[0] * es) % 16 != 0 || (p.sv[0] * es) % 16 != 0))) {
+        *why = "k and v rows must be 16-byte aligned"; return false;
+    }
+    int chunk, smem;
+    DecParams dp;
+    if (!plan_split(p, kSplitMaxCluster, &chunk, &dp, &smem)) {
+        *why = "the scores of a 1/16 key chunk do not fit shared memory"; return false;
+    }
+    return true;
+}
+
+cudaError_t launch_split(const Problem& p, cudaStream_t stream) {
+    const char* why;
+    if (!split_supports(p, &why)) return cudaErrorNotSupported;
+    switch (p.dtype) {
+        case kF32: return launch_split_t<float>(p, stream);
+        case kF16: return launch_split_t<__half>(p, stream);
+        case kBF16: return launch_split_t<__nv_bfloat16>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {

@@ -59,8 +59,10 @@ PREFILL_2K_D128_BF16 = Workload("prefill2k_d128_bf16", "bf16", 1, 16, 16, 2048, 
 GQA_1K_D128 = Workload("gqa1k_d128_f16", "f16", 1, 32, 8, 1024, 1024, 128, False, None, seed=3)
 DECODE = Workload("decode_skv1152_f16", "f16", 8, 32, 8, 1, 1152, 128, False, None, seed=4)
 TAIL100 = Workload("tail100_mask_f16", "f16", 4, 8, 8, 100, 100, 64, False, "bool_keep0.8_rows5pct", seed=5)
+# long-context decode (split-KV): the decode shape with a 32K-key cache
+DECODE_32K = Workload("decode_skv32k_f16", "f16", 8, 32, 8, 1, 32768, 128, False, None, seed=6)
 
-ALL = [TINY, PREFILL_1K_D64, PREFILL_2K_D128, PREFILL_2K_D128_BF16, GQA_1K_D128, DECODE, TAIL100]
+ALL = [TINY, PREFILL_1K_D64, PREFILL_2K_D128, PREFILL_2K_D128_BF16, GQA_1K_D128, DECODE, TAIL100, DECODE_32K]
 BY_NAME = {w.name: w for w in ALL}
 
 

@@ -68,7 +68,7 @@ def _full_check(q, k, v, mask, causal, scale, variant="auto", check_lse=True):
 def _variants_for(q, k, v, mask, causal):
     """Every kernel family that accepts this call (the SIMT one always does)."""
     out = []
-    for name in ("simt", "twopass", "paired", "fused", "decode"):
+    for name in ("simt", "twopass", "paired", "fused", "decode", "split"):
         try:
             sm.sdpa_math_plan(q, k, v, mask, is_causal=causal, variant=name)
             out.append(name)
@@ -79,7 +79,7 @@ def _variants_for(q, k, v, mask, causal):
 
 # --------------------------------------------------------------------------- workloads
 
-@pytest.mark.parametrize("w", [W.TINY, W.TAIL100, W.DECODE], ids=lambda w: w.name)
+@pytest.mark.parametrize("w", [W.TINY, W.TAIL100, W.DECODE, W.DECODE_32K], ids=lambda w: w.name)
 def test_workload_full_compare(w):
     q, k, v, m = W.make_inputs(w)
     for variant in ["auto"] + _variants_for(q, k, v, m, w.is_causal):
@@ -137,6 +137,15 @@ SMALL = [
     (1, 2, 2, 100, 100, 64, "bf16", False, "bool"),
     (1, 2, 1, 7, 1, 64, "f16", False, None),
     (1, 3, 3, 250, 129, 128, "bf16", False, "additive"),
+    # few rows per KV head over long key sequences (split-KV): ragged chunks
+    # and V sub-tiles, masks with fully masked rows, causal rows that see one
+    # key, 16 rows at D = 256, and fewer keys than CTAs in the cluster
+    (1, 4, 1, 1, 5000, 128, "f16", False, None),
+    (2, 8, 2, 2, 3001, 64, "bf16", False, "bool"),
+    (1, 2, 2, 8, 2500, 128, "f32", False, "additive"),
+    (1, 16, 1, 1, 4100, 256, "f16", False, None),
+    (1, 2, 1, 6, 2200, 64, "f16", True, None),
+    (1, 4, 1, 1, 10, 64, "f16", False, None),
 ]
 
 
