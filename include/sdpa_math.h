@@ -199,11 +199,27 @@ sdpa_status sdpa_math_device_status(sdpa_stream_t stream);
  * All tensors share one dtype (f32 / f16 / bf16, fp32 accumulation), device
  * pointers, unit innermost stride; D, Dv <= 256.  Asynchronous on `stream`.
  * Errors as sdpa_math_fwd (argument checks on the host before any launch).
+ * f16 / bf16 calls with D == Dv in {64, 128} and 16-byte aligned rows run on
+ * the tensor cores (two kernels: per query tile dq and rowsum, then per key
+ * tile dk and dv; dS is rounded to the input dtype as an MMA operand); every
+ * other call runs on two CUDA-core kernels with fp32 dS.
  */
 sdpa_status sdpa_math_bwd(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
                           const sdpa_tensor *probs, const sdpa_tensor *dout, const sdpa_tensor *dprobs,
                           float scale, sdpa_tensor *dq, sdpa_tensor *dk, sdpa_tensor *dv, float *rowsum,
                           sdpa_stream_t stream);
+
+/*
+ * sdpa_math_bwd_ex -- sdpa_math_bwd with the kernel family chosen by the
+ * caller: SDPA_VARIANT_AUTO (as sdpa_math_bwd), SDPA_VARIANT_SIMT (the
+ * CUDA-core kernels, any supported shape) or SDPA_VARIANT_TC_TWOPASS (the
+ * tensor-core kernels; SDPA_ERR_UNSUPPORTED with the reason when the call
+ * does not meet their conditions).  Any other value is SDPA_ERR_INVALID_ARGUMENT.
+ */
+sdpa_status sdpa_math_bwd_ex(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
+                             const sdpa_tensor *probs, const sdpa_tensor *dout, const sdpa_tensor *dprobs,
+                             float scale, sdpa_tensor *dq, sdpa_tensor *dk, sdpa_tensor *dv, float *rowsum,
+                             sdpa_variant variant, sdpa_stream_t stream);
 
 /*
  * sdpa_math_selftest_wait -- diagnostic for the failure path above.  Enqueues

@@ -23,7 +23,7 @@ from . import _build
 
 __all__ = [
     "sdpa_math", "sdpa_math_fwd", "sdpa_math_fwd_ex", "sdpa_math_plan",
-    "sdpa_math_bwd", "sdpa_math_backward", "sdpa_math_device_status", "sdpa_math_selftest_wait", "sdpa_math_last_error", "sdpa_math_abi_version",
+    "sdpa_math_bwd", "sdpa_math_backward", "BWD_VARIANTS", "sdpa_math_device_status", "sdpa_math_selftest_wait", "sdpa_math_last_error", "sdpa_math_abi_version",
     "SdpaError", "SdpaValueError", "load_library", "library_path", "VARIANTS", "STATUS",
 ]
 
@@ -96,6 +96,9 @@ def load_library(build_if_missing: bool = False):
         lib.sdpa_math_bwd.restype = ctypes.c_int
         lib.sdpa_math_bwd.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_void_p,
                                       ctypes.c_void_p]
+        lib.sdpa_math_bwd_ex.restype = ctypes.c_int
+        lib.sdpa_math_bwd_ex.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_void_p,
+                                         ctypes.c_int, ctypes.c_void_p]
         lib.sdpa_math_selftest_wait.restype = ctypes.c_int
         lib.sdpa_math_selftest_wait.argtypes = [ctypes.c_void_p]
         lib.sdpa_math_last_error.restype = ctypes.c_char_p
@@ -220,20 +223,32 @@ def sdpa_math_device_status(stream=None) -> None:
         _raise(lib, st)
 
 
-def sdpa_math_bwd(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, stream=None) -> None:
-    """Direct C-ABI backward on caller-allocated device tensors (raises on error)."""
+# Backward kernel families (sdpa_math_bwd_ex): "tc" = the tensor-core kernels.
+BWD_VARIANTS = {"auto": 0, "simt": 1, "tc": 2}
+
+
+def sdpa_math_bwd(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, stream=None,
+                  variant: str = "auto") -> None:
+    """Direct C-ABI backward on caller-allocated device tensors (raises on error).
+    ``variant`` "auto" calls sdpa_math_bwd; "simt" / "tc" force a family through
+    sdpa_math_bwd_ex."""
     lib = load_library()
     args = [describe(t) for t in (q, k, v, probs, dout)]
     dg = describe(dprobs) if dprobs is not None else None
     outs = [describe(t) for t in (dq, dk, dv)]
-    st = lib.sdpa_math_bwd(*(ctypes.byref(a) for a in args), ctypes.byref(dg) if dg is not None else None,
-                           float(scale), *(ctypes.byref(o) for o in outs),
-                           rowsum.data_ptr() if rowsum is not None else None, _stream_handle(stream))
+    common = [*(ctypes.byref(a) for a in args), ctypes.byref(dg) if dg is not None else None,
+              float(scale), *(ctypes.byref(o) for o in outs), rowsum.data_ptr() if rowsum is not None else None]
+    if variant == "auto":
+        st = lib.sdpa_math_bwd(*common, _stream_handle(stream))
+    else:
+        code = BWD_VARIANTS[variant] if isinstance(variant, str) else int(variant)
+        st = lib.sdpa_math_bwd_ex(*common, code, _stream_handle(stream))
     if st != SDPA_OK:
         _raise(lib, st)
 
 
-def sdpa_math_backward(q, k, v, probs, dout, dprobs=None, scale: Optional[float] = None, stream=None):
+def sdpa_math_backward(q, k, v, probs, dout, dprobs=None, scale: Optional[float] = None, stream=None,
+                       variant: str = "auto"):
     """(dq, dk, dv) of the (O, P) forward for gradients dout (of O) and dprobs
     (of P, optional), given the forward's P; CUDA tensors through the C ABI.
     Allocates the outputs and the per-row workspace (B*Hq*Sq floats)."""
@@ -242,7 +257,7 @@ def sdpa_math_backward(q, k, v, probs, dout, dprobs=None, scale: Optional[float]
         scale = 1.0 / math.sqrt(q.shape[-1]) if q.shape[-1] > 0 else 1.0
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     rowsum = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    sdpa_math_bwd(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, stream)
+    sdpa_math_bwd(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, stream, variant)
     return dq, dk, dv
 
 

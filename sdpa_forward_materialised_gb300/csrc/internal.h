@@ -74,7 +74,9 @@ bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 bool split_supports(const Problem& p, const char** why);
 cudaError_t launch_split(const Problem& p, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdProblem& p, cudaStream_t stream);
+cudaError_t launch_bwd(const BwdProblem& p, cudaStream_t stream);   // CUDA-core kernels, any shape
+bool bwd_tc_supports(const BwdProblem& p, const char** why);
+cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream);  // tensor-core kernels
 
 // Device error word shared by every kernel of the library (see
 // sdpa_math_device_status).  read_and_clear returns the word's old value.

@@ -323,11 +323,14 @@ sdpa_status sdpa_math_device_status(sdpa_stream_t stream) {
     return SDPA_OK;
 }
 
-sdpa_status sdpa_math_bwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
-                          const sdpa_tensor* probs, const sdpa_tensor* dout, const sdpa_tensor* dprobs,
-                          float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv, float* rowsum,
-                          sdpa_stream_t stream) {
+sdpa_status sdpa_math_bwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                             const sdpa_tensor* probs, const sdpa_tensor* dout, const sdpa_tensor* dprobs,
+                             float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv, float* rowsum,
+                             sdpa_variant variant, sdpa_stream_t stream) {
     g_last_error.clear();
+    if (variant != SDPA_VARIANT_AUTO && variant != SDPA_VARIANT_SIMT && variant != SDPA_VARIANT_TC_TWOPASS)
+        return fail(SDPA_ERR_INVALID_ARGUMENT, "backward variant must be AUTO, SIMT or TC_TWOPASS (got %d)",
+                    (int)variant);
     sdpa_status s;
     const sdpa_tensor* all[] = {q, k, v, probs, dout, dq, dk, dv};
     const char* names[] = {"q", "k", "v", "probs", "dout", "dq", "dk", "dv"};
@@ -375,10 +378,29 @@ sdpa_status sdpa_math_bwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa
     set(dv, &tmp, p.sdv); p.dv = dv->data;
     p.rowsum = rowsum;
     p.scale = scale;
+    const char* why = nullptr;
+    const bool tc_ok = sdpa::bwd_tc_supports(p, &why);
+    if (variant == SDPA_VARIANT_TC_TWOPASS && !tc_ok)
+        return fail(SDPA_ERR_UNSUPPORTED, "tensor-core backward cannot serve this call: %s", why);
     if (B * Hkv == 0 || (Sq == 0 && Skv == 0)) return SDPA_OK;
-    const cudaError_t e = sdpa::launch_bwd(p, reinterpret_cast<cudaStream_t>(stream));
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool use_tc = variant == SDPA_VARIANT_TC_TWOPASS || (variant == SDPA_VARIANT_AUTO && tc_ok);
+    cudaError_t e = use_tc ? sdpa::launch_bwd_tc(p, st) : sdpa::launch_bwd(p, st);
+    if (e == cudaErrorNotSupported && use_tc) {
+        (void)cudaGetLastError();
+        if (variant != SDPA_VARIANT_AUTO)
+            return fail(SDPA_ERR_UNSUPPORTED, "tensor-core backward refused its launch configuration");
+        e = sdpa::launch_bwd(p, st);
+    }
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     return SDPA_OK;
+}
+
+sdpa_status sdpa_math_bwd(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                          const sdpa_tensor* probs, const sdpa_tensor* dout, const sdpa_tensor* dprobs,
+                          float scale, sdpa_tensor* dq, sdpa_tensor* dk, sdpa_tensor* dv, float* rowsum,
+                          sdpa_stream_t stream) {
+    return sdpa_math_bwd_ex(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, SDPA_VARIANT_AUTO, stream);
 }
 
 sdpa_status sdpa_math_selftest_wait(sdpa_stream_t stream) {

@@ -1065,6 +1065,396 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     }
 }
 
+
+// ---------------------------------------------------------------- backward
+//
+// Gradients of the (O, P) forward for dout (of O) and dprobs (of P) given P
+// (FlagOS-OP PR #10, A1 item and the "P800 fused backward" update):
+//   dP = dO V^T + dprobs,  r = rowsum(P * dP),  dS = P * (dP - r),
+//   dQ = scale dS K,  dK = scale sum_h dS^T Q,  dV = sum_h P^T dO
+// (sums over the query heads of a key/value head).  Every product is a
+// tcgen05 MMA with fp32 accumulation in TMEM; dS is rounded to the input
+// type once, as the operand of the dQ and dK products.
+//   rows kernel: CTA per 128-row query tile of one head.  Sweep 1 over the
+//     key tiles forms dP in TMEM and r; sweep 2 forms dP again, dS, and
+//     accumulates dQ = dS K_j.  Writes dQ and r (the caller's row buffer).
+//   keys kernel: CTA per 128-key tile of one key/value head, looping over the
+//     group's query heads and query tiles: dP (lanes = queries), dS, then
+//     dV += P^T dO and dK += dS^T Q with the A operand read MN-major from the
+//     same [query][key] tiles, accumulated over the whole group in TMEM.
+// Operands are staged with asynchronous 16-byte copies into 128-byte-swizzled
+// tiles; [query][key] tiles (P, dprobs, dS) use the layout of the forward's
+// P operand, so one tile serves as K-major A (keys = K) and as MN-major A
+// (keys = M).  Only D == Dv in {64, 128} and 16-byte aligned rows.
+
+struct BwdIO {
+    const void* q; long long sq0, sq1, sq2;
+    const void* k; long long sk0, sk1, sk2;
+    const void* v; long long sv0, sv1, sv2;
+    const void* p; long long sp0, sp1, sp2;
+    const void* go; long long sgo0, sgo1, sgo2;
+    const void* gp; long long sgp0, sgp1, sgp2;  // dprobs, or null
+    void* dq; long long sdq0, sdq1, sdq2;
+    void* dk; long long sdk0, sdk1, sdk2;
+    void* dv; long long sdv0, sdv1, sdv2;
+    float* rowsum;  // [B, Hq, Sq] contiguous
+    int Hq, group, Sq, Skv;
+    float scale;
+};
+
+constexpr int kBwdThreads = 256;
+static_assert(kBwdThreads == FusedCfg::kThreads, "load_tile_sw128 strides by the fused kernel's block size");
+
+template <int D>
+struct BwdSmem {
+    static constexpr int kT = 128 * D * 2;      // [128, D] operand tile
+    static constexpr int kPT = 128 * 128 * 2;   // [128 queries, 128 keys] tile
+    static constexpr int kOffA = 0;             // rows kernel: dO_i   keys kernel: V_j
+    static constexpr int kOffB = kOffA + kT;    // rows kernel: V_j    keys kernel: dO_i
+    static constexpr int kOffC = kOffB + kT;    // rows kernel: K_j    keys kernel: Q_i
+    static constexpr int kOffP = kOffC + kT;
+    static constexpr int kOffG = kOffP + kPT;   // dprobs
+    static constexpr int kOffS = kOffG + kPT;   // dS
+    static constexpr int kOffStat = kOffS + kPT;
+    static constexpr int kOffBar = kOffStat + 1024;
+    static constexpr int kSmem = kOffBar + 64 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// 16-byte chunk c (keys 8c .. 8c+7) of row r of a swizzled [128, 128] tile.
+__device__ __forceinline__ uint32_t sw_chunk(uint32_t tile, int r, int c) {
+    return tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice (element row
+// stride srow, 16-byte aligned rows) into a swizzled [128, 128] tile; the rest
+// of the tile is zero-filled (partial chunks at the key edge included).
+template <typename T>
+__device__ __forceinline__ void load_ptile_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
+    for (int u = threadIdx.x; u < 128 * 16; u += kBwdThreads) {
+        const int r = u >> 4, c = u & 15;
+        int bytes = (ncols - 8 * c) * 2;
+        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
+        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sw_chunk(dst, r, c)), "l"(g), "r"(bytes)
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&w)[4]) {
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+}
+
+template <typename T> __device__ __forceinline__ float2 unpack_pair(uint32_t w);
+template <> __device__ __forceinline__ float2 unpack_pair<__half>(uint32_t w) {
+    return __half22float2(*reinterpret_cast<__half2*>(&w));
+}
+template <> __device__ __forceinline__ float2 unpack_pair<__nv_bfloat16>(uint32_t w) {
+    return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
+}
+
+// This thread's 64 keys (chunks c0 .. c0+7) of row t: reads dP (fp32, from
+// registers), P and dprobs (swizzled tiles); either accumulates sum P (dP + g)
+// into r_acc (dS == false) or writes dS = P (dP + g - r) to the dS tile.
+template <typename T, bool kDS>
+__device__ __forceinline__ void bwd_row_chunks(const float (&dp)[64], uint32_t sP, uint32_t sG, uint32_t sS, bool has_g,
+                                               int t, int c0, float r, float& r_acc) {
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t pw[4], gw[4] = {0u, 0u, 0u, 0u};
+        ld_shared_v4(sw_chunk(sP, t, c0 + c), pw);
+        if (has_g) ld_shared_v4(sw_chunk(sG, t, c0 + c), gw);
+        uint32_t out[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 pp = unpack_pair<T>(pw[e]), gg = unpack_pair<T>(gw[e]);
+            const float d0 = dp[8 * c + 2 * e] + gg.x, d1 = dp[8 * c + 2 * e + 1] + gg.y;
+            if constexpr (kDS) {
+                out[e] = Pack<T>::two(pp.x * (d0 - r), pp.y * (d1 - r));
+            } else {
+                acc = fmaf(pp.x, d0, acc);
+                acc = fmaf(pp.y, d1, acc);
+            }
+        }
+        if constexpr (kDS) st_shared_v4(sw_chunk(sS, t, c0 + c), out[0], out[1], out[2], out[3]);
+    }
+    r_acc += acc;
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+bwd_tc_rows_kernel(const BwdIO io) {
+    using L = BwdSmem<D>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kCols = 256;  // dP [0, 128), dQ [128, 128 + D)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sDO = smem_u32(smem + L::kOffA), sV = smem_u32(smem + L::kOffB), sK = smem_u32(smem + L::kOffC);
+    const uint32_t sP = smem_u32(smem + L::kOffP), sG = smem_u32(smem + L::kOffG), sS = smem_u32(smem + L::kOffS);
+    float* stat = reinterpret_cast<float*>(smem + L::kOffStat);  // [2 warpgroups][128] partial row sums
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
+    const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int hk = h / io.group, r0 = qt * 128;
+    const int nrows = min(128, io.Sq - r0);
+    const int n_kv = (io.Skv + 127) / 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t bar = smem_u32(&bars[0]);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kCols);
+        tmem_relinquish();
+    }
+    const T* DO = static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2;
+    const T* Pr = static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2;
+    const T* Gr = io.gp ? static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 + (long long)r0 * io.sgp2 : nullptr;
+    const T* Vb = static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1;
+    const T* Kb = static_cast<const T*>(io.k) + b * io.sk0 + hk * io.sk1;
+    load_tile_sw128<T>(sDO, DO, io.sgo2, nrows, D);  // completes with the first key tile's group
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t idesc_dp = idesc_f16(128, 128, kBF16, false);
+    constexpr uint32_t idesc_dq = idesc_f16(128, D, kBF16, true);
+    uint32_t phase = 0;
+    float r_acc = 0.f, r = 0.f;
+
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int j = 0; j < n_kv; ++j) {
+            const int j0 = j * 128, ncols = min(128, io.Skv - j0);
+            load_tile_sw128<T>(sV, Vb + (long long)j0 * io.sv2, io.sv2, ncols, D);
+            if (pass == 1) load_tile_sw128<T>(sK, Kb + (long long)j0 * io.sk2, io.sk2, ncols, D);
+            load_ptile_sw128<T>(sP, Pr + j0, io.sp2, nrows, ncols);
+            if (Gr) load_ptile_sw128<T>(sG, Gr + j0, io.sgp2, nrows, ncols);
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (threadIdx.x == 0) {  // dP = dO_i V_j^T
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    tc_mma_f16(tmem, sw128_desc(sDO + off, 16, 1024), sw128_desc(sV + off, 16, 1024), idesc_dp,
+                               kk > 0 ? 1u : 0u);
+                }
+                tc_commit(bar);
+            }
+            wait_bar(bar, phase, abort_flag, 8, 2 * pass);
+            phase ^= 1u;
+            tc_fence_after();
+            float dp[64];
+            tmem_ld32(tmem + lane_base + wg * 64, dp);
+            tmem_ld32(tmem + lane_base + wg * 64 + 32, dp + 32);
+            if (pass == 0) {
+                bwd_row_chunks<T, false>(dp, sP, sG, sS, Gr != nullptr, t, wg * 8, 0.f, r_acc);
+            } else {
+                float unused = 0.f;
+                bwd_row_chunks<T, true>(dp, sP, sG, sS, Gr != nullptr, t, wg * 8, r, unused);
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncthreads();
+                if (threadIdx.x == 0) {  // dQ += dS K_j
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;
+                        tc_mma_f16(tmem + 128, sw128_desc(sS + a_off, 16, 1024), sw128_desc(sK + kk * 2048, 16384, 1024),
+                                   idesc_dq, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc_commit(bar);
+                }
+                wait_bar(bar, phase, abort_flag, 8, 2 * pass + 1);
+                phase ^= 1u;
+                tc_fence_after();
+            }
+            __syncthreads();  // every read of this key tile's shared memory is done
+        }
+        if (pass == 0) {
+            stat[wg * 128 + t] = r_acc;
+            __syncthreads();
+            r = stat[t] + stat[128 + t];
+            if (wg == 0 && t < nrows) io.rowsum[((long long)b * io.Hq + h) * io.Sq + r0 + t] = r;
+        }
+    }
+
+    // dQ: warpgroup w writes columns [w D/2, (w+1) D/2) of row t
+    {
+        T* drow = static_cast<T*>(io.dq) + b * io.sdq0 + h * io.sdq1 + (long long)(r0 + t) * io.sdq2 + wg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + 128 + wg * (D / 2) + c * 32, v);
+            if (t < nrows) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 pk;
+                    pk.x = Pack<T>::two(io.scale * v[u * 8 + 0], io.scale * v[u * 8 + 1]);
+                    pk.y = Pack<T>::two(io.scale * v[u * 8 + 2], io.scale * v[u * 8 + 3]);
+                    pk.z = Pack<T>::two(io.scale * v[u * 8 + 4], io.scale * v[u * 8 + 5]);
+                    pk.w = Pack<T>::two(io.scale * v[u * 8 + 6], io.scale * v[u * 8 + 7]);
+                    *reinterpret_cast<uint4*>(drow + c * 32 + u * 8) = pk;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        if (*abort_flag)
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+bwd_tc_keys_kernel(const BwdIO io) {
+    using L = BwdSmem<D>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kCols = 128 + 2 * D <= 256 ? 256 : 512;  // dP [0,128), dV [128,128+D), dK after
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sV = smem_u32(smem + L::kOffA), sDO = smem_u32(smem + L::kOffB), sQ = smem_u32(smem + L::kOffC);
+    const uint32_t sP = smem_u32(smem + L::kOffP), sG = smem_u32(smem + L::kOffG), sS = smem_u32(smem + L::kOffS);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
+    const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const int j0 = kt * 128, ncols = min(128, io.Skv - j0);
+    const int nq = (io.Sq + 127) / 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t bar = smem_u32(&bars[0]);
+    const uint32_t tDV = 128, tDK = 128 + D;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kCols);
+        tmem_relinquish();
+    }
+    load_tile_sw128<T>(sV, static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1 + (long long)j0 * io.sv2, io.sv2,
+                       ncols, D);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    constexpr uint32_t idesc_dp = idesc_f16(128, 128, kBF16, false);
+    constexpr uint32_t idesc_kv = idesc_f16(128, D, kBF16, true) | (1u << 15);  // A MN-major too
+    uint32_t phase = 0;
+    int it = 0;
+
+    for (int g = 0; g < io.group; ++g) {
+        const int h = hk * io.group + g;
+        for (int i = 0; i < nq; ++i, ++it) {
+            const int r0 = i * 128, nrows = min(128, io.Sq - r0);
+            load_tile_sw128<T>(sDO, static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2,
+                               io.sgo2, nrows, D);
+            load_tile_sw128<T>(sQ, static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2,
+                               io.sq2, nrows, D);
+            load_ptile_sw128<T>(sP, static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2 + j0,
+                                io.sp2, nrows, ncols);
+            if (io.gp)
+                load_ptile_sw128<T>(sG,
+                                    static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 +
+                                        (long long)r0 * io.sgp2 + j0,
+                                    io.sgp2, nrows, ncols);
+            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            tc_fence_after();
+            if (threadIdx.x == 0) {
+                // dP = dO_i V_j^T (lanes = queries, columns = keys)
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                    tc_mma_f16(tmem, sw128_desc(sDO + off, 16, 1024), sw128_desc(sV + off, 16, 1024), idesc_dp,
+                               kk > 0 ? 1u : 0u);
+                }
+                // dV += P_i^T dO_i (lanes = keys): both operands MN-major, K = queries
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16(tmem + tDV, sw128_desc(sP + kk * 2048, 16384, 1024),
+                               sw128_desc(sDO + kk * 2048, 16384, 1024), idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar);
+            }
+            wait_bar(bar, phase, abort_flag, 9, 0);
+            phase ^= 1u;
+            tc_fence_after();
+            float dp[64];
+            tmem_ld32(tmem + lane_base + wg * 64, dp);
+            tmem_ld32(tmem + lane_base + wg * 64 + 32, dp + 32);
+            const float r = t < nrows ? io.rowsum[((long long)b * io.Hq + h) * io.Sq + r0 + t] : 0.f;
+            float unused = 0.f;
+            bwd_row_chunks<T, true>(dp, sP, sG, sS, io.gp != nullptr, t, wg * 8, r, unused);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+            if (threadIdx.x == 0) {  // dK += dS_i^T Q_i
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_f16(tmem + tDK, sw128_desc(sS + kk * 2048, 16384, 1024),
+                               sw128_desc(sQ + kk * 2048, 16384, 1024), idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar);
+            }
+            wait_bar(bar, phase, abort_flag, 9, 1);
+            phase ^= 1u;
+            tc_fence_after();
+            __syncthreads();  // every read of this query tile's shared memory is done
+        }
+    }
+
+    // dV (warpgroup 0) and dK (warpgroup 1) rows: lane t is key j0 + t
+    {
+        const bool is_k = wg == 1;
+        T* drow = is_k ? static_cast<T*>(io.dk) + b * io.sdk0 + hk * io.sdk1 + (long long)(j0 + t) * io.sdk2
+                       : static_cast<T*>(io.dv) + b * io.sdv0 + hk * io.sdv1 + (long long)(j0 + t) * io.sdv2;
+        const float sc = is_k ? io.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+            float v[32];
+            tmem_ld32(tmem + lane_base + (is_k ? tDK : tDV) + c * 32, v);
+            if (t < ncols) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    uint4 pk;
+                    pk.x = Pack<T>::two(sc * v[u * 8 + 0], sc * v[u * 8 + 1]);
+                    pk.y = Pack<T>::two(sc * v[u * 8 + 2], sc * v[u * 8 + 3]);
+                    pk.z = Pack<T>::two(sc * v[u * 8 + 4], sc * v[u * 8 + 5]);
+                    pk.w = Pack<T>::two(sc * v[u * 8 + 6], sc * v[u * 8 + 7]);
+                    *reinterpret_cast<uint4*>(drow + c * 32 + u * 8) = pk;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        if (*abort_flag)
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1348,6 +1738,66 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
         *why = "outer strides must be multiples of 8 elements (16 bytes)"; return false;
     }
     return true;
+}
+
+bool bwd_tc_supports(const BwdProblem& p, const char** why) {
+    if (p.dtype != kF16 && p.dtype != kBF16) { *why = "dtype must be f16 or bf16"; return false; }
+    if (p.D != p.Dv || (p.D != 64 && p.D != 128)) { *why = "head dim must be 64 or 128 (D == Dv)"; return false; }
+    if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
+    if (p.Sq >= (1ll << 31) || p.Skv >= (1ll << 31) || p.B > 65535 || p.Hq > 65535) {
+        *why = "sizes beyond the grid limits"; return false;
+    }
+    const void* ptrs[9] = {p.q, p.k, p.v, p.p, p.dout, p.dprobs, p.dq, p.dk, p.dv};
+    for (const void* x : ptrs)
+        if (x && !aligned16(x)) { *why = "every tensor must be 16-byte aligned"; return false; }
+    const int64_t eq[3] = {p.B, p.Hq, p.Sq}, ek[3] = {p.B, p.Hkv, p.Skv};
+    if (!strides_ok(p.sq, eq) || !strides_ok(p.sk, ek) || !strides_ok(p.sv, ek) || !strides_ok(p.sp, eq) ||
+        !strides_ok(p.sgo, eq) || (p.dprobs && !strides_ok(p.sgp, eq)) || !strides_ok(p.sdq, eq) ||
+        !strides_ok(p.sdk, ek) || !strides_ok(p.sdv, ek)) {
+        *why = "rows must start on 16-byte boundaries"; return false;
+    }
+    // P and dprobs rows are read in 16-byte chunks from their own start
+    if ((p.Sq > 1 && p.sp[2] % 8 != 0) || (p.dprobs && p.Sq > 1 && p.sgp[2] % 8 != 0)) {
+        *why = "probs and dprobs rows must start on 16-byte boundaries"; return false;
+    }
+    return true;
+}
+
+namespace {
+template <int D, typename T>
+cudaError_t launch_bwd_tc_t(const BwdProblem& p, cudaStream_t stream) {
+    BwdIO io;
+    std::memset(&io, 0, sizeof(io));
+    io.q = p.q; io.sq0 = p.sq[0]; io.sq1 = p.sq[1]; io.sq2 = p.sq[2];
+    io.k = p.k; io.sk0 = p.sk[0]; io.sk1 = p.sk[1]; io.sk2 = p.sk[2];
+    io.v = p.v; io.sv0 = p.sv[0]; io.sv1 = p.sv[1]; io.sv2 = p.sv[2];
+    io.p = p.p; io.sp0 = p.sp[0]; io.sp1 = p.sp[1]; io.sp2 = p.sp[2];
+    io.go = p.dout; io.sgo0 = p.sgo[0]; io.sgo1 = p.sgo[1]; io.sgo2 = p.sgo[2];
+    io.gp = p.dprobs; io.sgp0 = p.sgp[0]; io.sgp1 = p.sgp[1]; io.sgp2 = p.sgp[2];
+    io.dq = p.dq; io.sdq0 = p.sdq[0]; io.sdq1 = p.sdq[1]; io.sdq2 = p.sdq[2];
+    io.dk = p.dk; io.sdk0 = p.sdk[0]; io.sdk1 = p.sdk[1]; io.sdk2 = p.sdk[2];
+    io.dv = p.dv; io.sdv0 = p.sdv[0]; io.sdv1 = p.sdv[1]; io.sdv2 = p.sdv[2];
+    io.rowsum = p.rowsum;
+    io.Hq = (int)p.Hq; io.group = (int)p.group; io.Sq = (int)p.Sq; io.Skv = (int)p.Skv;
+    io.scale = p.scale;
+    constexpr int smem = BwdSmem<D>::kSmem;
+    auto kr = bwd_tc_rows_kernel<D, T>;
+    auto kk = bwd_tc_keys_kernel<D, T>;
+    cudaError_t e = prepare_kernel(kr, smem, false);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare_kernel(kk, smem, false)) != cudaSuccess) return e;
+    kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    kk<<<dim3((unsigned)((p.Skv + 127) / 128), (unsigned)p.Hkv, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream) {
+    const char* why;
+    if (!bwd_tc_supports(p, &why)) return cudaErrorNotSupported;
+    if (p.dtype == kF16) return p.D == 64 ? launch_bwd_tc_t<64, __half>(p, stream) : launch_bwd_tc_t<128, __half>(p, stream);
+    return p.D == 64 ? launch_bwd_tc_t<64, __nv_bfloat16>(p, stream) : launch_bwd_tc_t<128, __nv_bfloat16>(p, stream);
 }
 
 cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream) {

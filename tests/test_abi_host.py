@@ -261,6 +261,28 @@ def _bwd_args(B=1, Hq=4, Hkv=2, Sq=9, Skv=11, D=16, Dv=8, dtype=torch.float16):
     return q, k, v, P, go, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
 
 
+def test_backward_variant_refusals(lib):
+    """sdpa_math_bwd_ex: the tensor-core family refuses what it cannot serve
+    (with the reason) before launching; unknown families are argument errors."""
+    q, k, v, P, go, dq, dk, dv = _bwd_args(Hq=4, Hkv=2, Sq=9, Skv=16, D=64, Dv=64)
+    rs = torch.zeros(1, 4, 9)
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_bwd(q, k, v, P, go, None, 0.25, dq, dk, dv, rs, stream=0, variant=7),
+            "backward variant")
+    q2, k2, v2, P2, go2, dq2, dk2, dv2 = _bwd_args(Hq=4, Hkv=2, Sq=9, Skv=16, D=64, Dv=32)
+    _expect("SDPA_ERR_UNSUPPORTED",
+            lambda: sm.sdpa_math_bwd(q2, k2, v2, P2, go2, None, 0.25, dq2, dk2, dv2, rs, stream=0, variant="tc"),
+            "D == Dv")
+    q3, k3, v3, P3, go3, dq3, dk3, dv3 = _bwd_args(Hq=4, Hkv=2, Sq=9, Skv=13, D=64, Dv=64)
+    _expect("SDPA_ERR_UNSUPPORTED",
+            lambda: sm.sdpa_math_bwd(q3, k3, v3, P3, go3, None, 0.25, dq3, dk3, dv3, rs, stream=0, variant="tc"),
+            "16-byte")
+    q4, k4, v4, P4, go4, dq4, dk4, dv4 = _bwd_args(Hq=4, Hkv=2, Sq=9, Skv=16, D=64, Dv=64, dtype=torch.float32)
+    _expect("SDPA_ERR_UNSUPPORTED",
+            lambda: sm.sdpa_math_bwd(q4, k4, v4, P4, go4, None, 0.25, dq4, dk4, dv4, rs, stream=0, variant="tc"),
+            "f16 or bf16")
+
+
 def test_backward_argument_errors(lib):
     """Host-side checks of sdpa_math_bwd (they return before any launch; the
     stream handle is never used on these paths)."""
