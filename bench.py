@@ -423,6 +423,12 @@ def bwd_bytes(w: W.Workload) -> int:
     return e * (3 * rows * w.D + 4 * w.B * w.Hkv * w.Skv * w.D + 2 * rows * w.Skv) + 4 * rows
 
 
+def bwd_tc_eligible(w: W.Workload) -> bool:
+    """Whether sdpa_math_bwd runs this workload on the tensor-core kernels
+    (f16/bf16, D == Dv in {64, 128}, contiguous P rows on 16-byte boundaries)."""
+    return w.dtype in ("f16", "bf16") and w.D in (64, 128) and w.Skv % 8 == 0
+
+
 def oracle_bwd_sample_ms(w: W.Workload, q, k, v, P, go, gp):
     """The oracle backward on one (batch, KV head) group, extrapolated to all
     B * Hkv groups (groups are independent and equal in size)."""
@@ -533,7 +539,8 @@ def run_ours_bwd(args, w: W.Workload):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": {"workload": w.name, "pass": "bwd", "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq,
                    "Skv": w.Skv, "D": w.D, "is_causal": w.is_causal, "mask": w.mask, "seed": w.seed,
-                   "kernels": "CUDA-core rows + keys kernels",
+                   "kernels": ("tensor-core (tcgen05) rows + keys kernels" if bwd_tc_eligible(w)
+                               else "CUDA-core rows + keys kernels"),
                    "l2": "flushed before every step (256 MiB write, then 256 MiB read)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_gbs": gbs, "algorithmic_bytes": nbytes,

@@ -1182,16 +1182,71 @@ __device__ __forceinline__ void bwd_row_chunks(const float (&dp)[64], uint32_t s
     r_acc += acc;
 }
 
+// Rows [0, nvalid) of a [rows, X] slice into a ROWS-row swizzled tile whose
+// 64-column halves sit ROWS * 128 bytes apart (rows past nvalid zero-filled).
+template <typename T, int ROWS>
+__device__ __forceinline__ void load_rows_sw128(uint32_t dst, const T* src, long long srow, int nvalid, int X) {
+    const int upr = X / 8;  // 16-byte units per row
+    for (int u = threadIdx.x; u < ROWS * upr; u += kBwdThreads) {
+        const int r = u / upr, c = u % upr;
+        const bool ok = r < nvalid;
+        const T* g = ok ? src + r * srow + c * 8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         dst + (c >> 3) * (ROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                     "l"(g), "r"(ok ? 16 : 0)
+                     : "memory");
+    }
+}
+
+// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice into a swizzled
+// [128, 64] tile (one 64-key half; partial chunks at the key edge zero-filled).
+template <typename T>
+__device__ __forceinline__ void load_ptile64_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
+    for (int u = threadIdx.x; u < 128 * 8; u += kBwdThreads) {
+        const int r = u >> 3, c = u & 7;
+        int bytes = (ncols - 8 * c) * 2;
+        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
+        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sw_chunk(dst, r, c)), "l"(g), "r"(bytes)
+                     : "memory");
+    }
+}
+
+// Rows kernel layout: dO once, then a three-stage ring of 64-key steps
+// (V_j K-major, K_j MN-major, P_ij and dprobs_ij; E hi / lo overwrite the last two).
+template <int D>
+struct BwdRowsSmem {
+    static constexpr int kStages = 3;
+    static constexpr int kKeys = 64;
+    static constexpr int kKV = kKeys * D * 2;     // [64, D] tile
+    static constexpr int kPG = 128 * kKeys * 2;   // [128, 64] tile
+    static constexpr int kStage = 2 * kKV + 2 * kPG;
+    static constexpr int kOffDO = 0;
+    static constexpr int kOffRing = 128 * D * 2;
+    static constexpr int kOffStat = kOffRing + kStages * kStage;
+    static constexpr int kOffBar = kOffStat + 1024;
+    static constexpr int kSmem = kOffBar + 64 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+    static_assert(kKV % 1024 == 0 && kPG % 1024 == 0, "tiles on 1024-byte boundaries");
+};
+
+// One sweep over the keys.  With E = P * (dP + dprobs) (fp32),
+//   r = rowsum(E),  dQ = scale (sum_j E_j K_j - r sum_j P_j K_j),
+// which equals scale * dS K without knowing r during the sweep.  E enters the
+// MMA as two rounded parts, E_hi = rn(E) and E_lo = rn(E - E_hi), so the
+// product is accurate to about fp32 and the final subtraction loses nothing
+// beyond fp32 rounding.  TMEM: dP [0, 64), A = sum E K [64, 64 + D),
+// Bp = sum P K [64 + D, 64 + 2D).
 template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_tc_rows_kernel(const BwdIO io) {
-    using L = BwdSmem<D>;
+    using L = BwdRowsSmem<D>;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr uint32_t kCols = 256;  // dP [0, 128), dQ [128, 128 + D)
+    constexpr uint32_t kCols = 64 + 2 * D <= 256 ? 256 : 512;
+    constexpr uint32_t tA = 64, tB = 64 + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sDO = smem_u32(smem + L::kOffA), sV = smem_u32(smem + L::kOffB), sK = smem_u32(smem + L::kOffC);
-    const uint32_t sP = smem_u32(smem + L::kOffP), sG = smem_u32(smem + L::kOffG), sS = smem_u32(smem + L::kOffS);
+    const uint32_t sDO = smem_u32(smem + L::kOffDO), sRing = smem_u32(smem + L::kOffRing);
     float* stat = reinterpret_cast<float*>(smem + L::kOffStat);  // [2 warpgroups][128] partial row sums
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
@@ -1201,7 +1256,7 @@ bwd_tc_rows_kernel(const BwdIO io) {
     const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int hk = h / io.group, r0 = qt * 128;
     const int nrows = min(128, io.Sq - r0);
-    const int n_kv = (io.Skv + 127) / 128;
+    const int nsteps = (io.Skv + L::kKeys - 1) / L::kKeys;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t bar = smem_u32(&bars[0]);
 
@@ -1219,90 +1274,130 @@ bwd_tc_rows_kernel(const BwdIO io) {
     const T* Gr = io.gp ? static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 + (long long)r0 * io.sgp2 : nullptr;
     const T* Vb = static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1;
     const T* Kb = static_cast<const T*>(io.k) + b * io.sk0 + hk * io.sk1;
-    load_tile_sw128<T>(sDO, DO, io.sgo2, nrows, D);  // completes with the first key tile's group
+    auto stage_v = [&](int st) { return sRing + st * L::kStage; };
+    auto stage_k = [&](int st) { return sRing + st * L::kStage + L::kKV; };
+    auto stage_p = [&](int st) { return sRing + st * L::kStage + 2 * L::kKV; };
+    auto stage_g = [&](int st) { return sRing + st * L::kStage + 2 * L::kKV + L::kPG; };
+    // one commit group per step (empty past the last step)
+    auto issue = [&](int step) {
+        if (step < nsteps) {
+            const int st = step % L::kStages, j0 = step * L::kKeys, nk = min(L::kKeys, io.Skv - j0);
+            load_rows_sw128<T, 64>(stage_v(st), Vb + (long long)j0 * io.sv2, io.sv2, nk, D);
+            load_rows_sw128<T, 64>(stage_k(st), Kb + (long long)j0 * io.sk2, io.sk2, nk, D);
+            load_ptile64_sw128<T>(stage_p(st), Pr + j0, io.sp2, nrows, nk);
+            if (Gr) load_ptile64_sw128<T>(stage_g(st), Gr + j0, io.sgp2, nrows, nk);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    load_tile_sw128<T>(sDO, DO, io.sgo2, nrows, D);  // joins step 0's group
+    issue(0);
+    issue(1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t idesc_dp = idesc_f16(128, 128, kBF16, false);
-    constexpr uint32_t idesc_dq = idesc_f16(128, D, kBF16, true);
+    constexpr uint32_t idesc_dp = idesc_f16(128, 64, kBF16, false);
+    constexpr uint32_t idesc_pk = idesc_f16(128, D, kBF16, true);
     uint32_t phase = 0;
-    float r_acc = 0.f, r = 0.f;
+    float r_acc = 0.f;
 
-    for (int pass = 0; pass < 2; ++pass) {
-        for (int j = 0; j < n_kv; ++j) {
-            const int j0 = j * 128, ncols = min(128, io.Skv - j0);
-            load_tile_sw128<T>(sV, Vb + (long long)j0 * io.sv2, io.sv2, ncols, D);
-            if (pass == 1) load_tile_sw128<T>(sK, Kb + (long long)j0 * io.sk2, io.sk2, ncols, D);
-            load_ptile_sw128<T>(sP, Pr + j0, io.sp2, nrows, ncols);
-            if (Gr) load_ptile_sw128<T>(sG, Gr + j0, io.sgp2, nrows, ncols);
-            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (threadIdx.x == 0) {  // dP = dO_i V_j^T
+    for (int step = 0; step < nsteps; ++step) {
+        const int st = step % L::kStages;
+        const uint32_t sV = stage_v(st), sK = stage_k(st), sP = stage_p(st), sG = stage_g(st);
+        issue(step + 2);
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (threadIdx.x == 0) {
+            // dP = dO V_j^T (N = 64 keys)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    tc_mma_f16(tmem, sw128_desc(sDO + off, 16, 1024), sw128_desc(sV + off, 16, 1024), idesc_dp,
-                               kk > 0 ? 1u : 0u);
-                }
-                tc_commit(bar);
-            }
-            wait_bar(bar, phase, abort_flag, 8, 2 * pass);
-            phase ^= 1u;
-            tc_fence_after();
-            float dp[64];
-            tmem_ld32(tmem + lane_base + wg * 64, dp);
-            tmem_ld32(tmem + lane_base + wg * 64 + 32, dp + 32);
-            if (pass == 0) {
-                bwd_row_chunks<T, false>(dp, sP, sG, sS, Gr != nullptr, t, wg * 8, 0.f, r_acc);
-            } else {
-                float unused = 0.f;
-                bwd_row_chunks<T, true>(dp, sP, sG, sS, Gr != nullptr, t, wg * 8, r, unused);
-                fence_proxy_async_smem();
-                tc_fence_before();
-                __syncthreads();
-                if (threadIdx.x == 0) {  // dQ += dS K_j
-                    tc_fence_after();
+            for (int kk = 0; kk < D / 16; ++kk)
+                tc_mma_f16(tmem, sw128_desc(sDO + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                           sw128_desc(sV + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idesc_dp, kk > 0 ? 1u : 0u);
+            // Bp += P_j K_j (K = 64 keys)
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t a_off = (kk / 4) * 16384 + (kk % 4) * 32;
-                        tc_mma_f16(tmem + 128, sw128_desc(sS + a_off, 16, 1024), sw128_desc(sK + kk * 2048, 16384, 1024),
-                                   idesc_dq, (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    tc_commit(bar);
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + tB, sw128_desc(sP + kk * 32, 16, 1024), sw128_desc(sK + kk * 2048, 8192, 1024),
+                           idesc_pk, (step > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar);
+        }
+        wait_bar(bar, phase, abort_flag, 8, 0);
+        phase ^= 1u;
+        tc_fence_after();
+        {
+            // this warpgroup's 32 keys (chunks 4 wg .. 4 wg + 3) of row t
+            float dp[32];
+            tmem_ld32(tmem + lane_base + wg * 32, dp);
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t ap = sw_chunk(sP, t, 4 * wg + c), ag = sw_chunk(sG, t, 4 * wg + c);
+                uint32_t pw[4], gw[4] = {0u, 0u, 0u, 0u};
+                ld_shared_v4(ap, pw);
+                if (Gr) ld_shared_v4(ag, gw);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 pp = unpack_pair<T>(pw[e]), gg = unpack_pair<T>(gw[e]);
+                    const float e0 = pp.x * (dp[8 * c + 2 * e] + gg.x), e1 = pp.y * (dp[8 * c + 2 * e + 1] + gg.y);
+                    acc += e0 + e1;
+                    hi[e] = Pack<T>::two(e0, e1);
+                    const float2 hh = unpack_pair<T>(hi[e]);
+                    lo[e] = Pack<T>::two(e0 - hh.x, e1 - hh.y);
                 }
-                wait_bar(bar, phase, abort_flag, 8, 2 * pass + 1);
-                phase ^= 1u;
-                tc_fence_after();
+                st_shared_v4(ap, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(ag, lo[0], lo[1], lo[2], lo[3]);
             }
-            __syncthreads();  // every read of this key tile's shared memory is done
+            r_acc += acc;
         }
-        if (pass == 0) {
-            stat[wg * 128 + t] = r_acc;
-            __syncthreads();
-            r = stat[t] + stat[128 + t];
-            if (wg == 0 && t < nrows) io.rowsum[((long long)b * io.Hq + h) * io.Sq + r0 + t] = r;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            tc_fence_after();
+            // A += E_hi K_j + E_lo K_j
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + tA, sw128_desc(sP + kk * 32, 16, 1024), sw128_desc(sK + kk * 2048, 8192, 1024),
+                           idesc_pk, (step > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + tA, sw128_desc(sG + kk * 32, 16, 1024), sw128_desc(sK + kk * 2048, 8192, 1024),
+                           idesc_pk, 1u);
+            tc_commit(bar);
         }
+        wait_bar(bar, phase, abort_flag, 8, 1);  // stage st and the dP columns are free again
+        phase ^= 1u;
+        tc_fence_after();
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 
-    // dQ: warpgroup w writes columns [w D/2, (w+1) D/2) of row t
+    stat[wg * 128 + t] = r_acc;
+    __syncthreads();
+    const float r = stat[t] + stat[128 + t];
+    if (wg == 0 && t < nrows) io.rowsum[((long long)b * io.Hq + h) * io.Sq + r0 + t] = r;
+
+    // dQ = scale (A - r Bp): warpgroup w writes columns [w D/2, (w+1) D/2) of row t
     {
         T* drow = static_cast<T*>(io.dq) + b * io.sdq0 + h * io.sdq1 + (long long)(r0 + t) * io.sdq2 + wg * (D / 2);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-            float v[32];
-            tmem_ld32(tmem + lane_base + 128 + wg * (D / 2) + c * 32, v);
+            float va[32], vb[32];
+            tmem_ld32(tmem + lane_base + tA + wg * (D / 2) + c * 32, va);
+            tmem_ld32(tmem + lane_base + tB + wg * (D / 2) + c * 32, vb);
             if (t < nrows) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = io.scale * fmaf(-r, vb[u * 8 + e], va[u * 8 + e]);
                     uint4 pk;
-                    pk.x = Pack<T>::two(io.scale * v[u * 8 + 0], io.scale * v[u * 8 + 1]);
-                    pk.y = Pack<T>::two(io.scale * v[u * 8 + 2], io.scale * v[u * 8 + 3]);
-                    pk.z = Pack<T>::two(io.scale * v[u * 8 + 4], io.scale * v[u * 8 + 5]);
-                    pk.w = Pack<T>::two(io.scale * v[u * 8 + 6], io.scale * v[u * 8 + 7]);
+                    pk.x = Pack<T>::two(o[0], o[1]);
+                    pk.y = Pack<T>::two(o[2], o[3]);
+                    pk.z = Pack<T>::two(o[4], o[5]);
+                    pk.w = Pack<T>::two(o[6], o[7]);
                     *reinterpret_cast<uint4*>(drow + c * 32 + u * 8) = pk;
                 }
             }
@@ -1780,13 +1875,13 @@ cudaError_t launch_bwd_tc_t(const BwdProblem& p, cudaStream_t stream) {
     io.rowsum = p.rowsum;
     io.Hq = (int)p.Hq; io.group = (int)p.group; io.Sq = (int)p.Sq; io.Skv = (int)p.Skv;
     io.scale = p.scale;
-    constexpr int smem = BwdSmem<D>::kSmem;
+    constexpr int smem = BwdSmem<D>::kSmem, smem_rows = BwdRowsSmem<D>::kSmem;
     auto kr = bwd_tc_rows_kernel<D, T>;
     auto kk = bwd_tc_keys_kernel<D, T>;
-    cudaError_t e = prepare_kernel(kr, smem, false);
+    cudaError_t e = prepare_kernel(kr, smem_rows, false);
     if (e != cudaSuccess) return e;
     if ((e = prepare_kernel(kk, smem, false)) != cudaSuccess) return e;
-    kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
+    kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem_rows, stream>>>(io);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kk<<<dim3((unsigned)((p.Skv + 127) / 128), (unsigned)p.Hkv, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
     return cudaGetLastError();
