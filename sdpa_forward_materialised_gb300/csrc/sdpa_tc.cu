@@ -112,12 +112,18 @@ template <> struct Pack<__half> {
         __half2 h = __floats2half2_rn(a, b);
         return *reinterpret_cast<uint32_t*>(&h);
     }
+    static __device__ __forceinline__ float load_bits(uint32_t bits) {
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(bits)));
+    }
     static __device__ __forceinline__ float load(const void* p) { return __half2float(*(const __half*)p); }
 };
 template <> struct Pack<__nv_bfloat16> {
     static __device__ __forceinline__ uint32_t two(float a, float b) {
         __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
         return *reinterpret_cast<uint32_t*>(&h);
+    }
+    static __device__ __forceinline__ float load_bits(uint32_t bits) {
+        return __uint_as_float(bits << 16);
     }
     static __device__ __forceinline__ float load(const void* p) {
         return __bfloat162float(*(const __nv_bfloat16*)p);
@@ -1073,19 +1079,20 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
 //   dP = dO V^T + dprobs,  r = rowsum(P * dP),  dS = P * (dP - r),
 //   dQ = scale dS K,  dK = scale sum_h dS^T Q,  dV = sum_h P^T dO
 // (sums over the query heads of a key/value head).  Every product is a
-// tcgen05 MMA with fp32 accumulation in TMEM; dS is rounded to the input
-// type once, as the operand of the dQ and dK products.
-//   rows kernel: CTA per 128-row query tile of one head.  Sweep 1 over the
-//     key tiles forms dP in TMEM and r; sweep 2 forms dP again, dS, and
-//     accumulates dQ = dS K_j.  Writes dQ and r (the caller's row buffer).
-//   keys kernel: CTA per 128-key tile of one key/value head, looping over the
-//     group's query heads and query tiles: dP (lanes = queries), dS, then
-//     dV += P^T dO and dK += dS^T Q with the A operand read MN-major from the
-//     same [query][key] tiles, accumulated over the whole group in TMEM.
+// tcgen05 MMA with fp32 accumulation in TMEM.
+//   rows kernel: CTA per 128-row query tile of one head, one sweep over the
+//     keys in 64-key steps: r and dQ through E = P * (dP + dprobs) (see the
+//     kernel).  Writes dQ and r (the caller's row buffer).
+//   keys kernel: CTA per 128-key tile of one key/value head, stepping over the
+//     group's query heads in 64-row query tiles: dP^T (lanes = keys), dS^T
+//     rounded to the input type, dV += P^T dO and dK += dS^T Q, accumulated
+//     over the whole group in TMEM.
 // Operands are staged with asynchronous 16-byte copies into 128-byte-swizzled
-// tiles; [query][key] tiles (P, dprobs, dS) use the layout of the forward's
-// P operand, so one tile serves as K-major A (keys = K) and as MN-major A
-// (keys = M).  Only D == Dv in {64, 128} and 16-byte aligned rows.
+// tiles through multi-stage rings; a [query][key] tile (P, dprobs) serves as a
+// K-major A operand (keys = K) and as an MN-major one (keys = M).  Separate
+// mbarriers for the two MMA groups of a step let the second group of one step
+// run under the start of the next.  Only D == Dv in {64, 128} and 16-byte
+// aligned rows.
 
 struct BwdIO {
     const void* q; long long sq0, sq1, sq2;
@@ -1105,41 +1112,12 @@ struct BwdIO {
 constexpr int kBwdThreads = 256;
 static_assert(kBwdThreads == FusedCfg::kThreads, "load_tile_sw128 strides by the fused kernel's block size");
 
-template <int D>
-struct BwdSmem {
-    static constexpr int kT = 128 * D * 2;      // [128, D] operand tile
-    static constexpr int kPT = 128 * 128 * 2;   // [128 queries, 128 keys] tile
-    static constexpr int kOffA = 0;             // rows kernel: dO_i   keys kernel: V_j
-    static constexpr int kOffB = kOffA + kT;    // rows kernel: V_j    keys kernel: dO_i
-    static constexpr int kOffC = kOffB + kT;    // rows kernel: K_j    keys kernel: Q_i
-    static constexpr int kOffP = kOffC + kT;
-    static constexpr int kOffG = kOffP + kPT;   // dprobs
-    static constexpr int kOffS = kOffG + kPT;   // dS
-    static constexpr int kOffStat = kOffS + kPT;
-    static constexpr int kOffBar = kOffStat + 1024;
-    static constexpr int kSmem = kOffBar + 64 + 1024;
-    static_assert(kSmem <= 227 * 1024, "shared memory budget");
-};
 
 // 16-byte chunk c (keys 8c .. 8c+7) of row r of a swizzled [128, 128] tile.
 __device__ __forceinline__ uint32_t sw_chunk(uint32_t tile, int r, int c) {
     return tile + (c >> 3) * 16384 + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice (element row
-// stride srow, 16-byte aligned rows) into a swizzled [128, 128] tile; the rest
-// of the tile is zero-filled (partial chunks at the key edge included).
-template <typename T>
-__device__ __forceinline__ void load_ptile_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
-    for (int u = threadIdx.x; u < 128 * 16; u += kBwdThreads) {
-        const int r = u >> 4, c = u & 15;
-        int bytes = (ncols - 8 * c) * 2;
-        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
-        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sw_chunk(dst, r, c)), "l"(g), "r"(bytes)
-                     : "memory");
-    }
-}
 
 __device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&w)[4]) {
     asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
@@ -1153,34 +1131,6 @@ template <> __device__ __forceinline__ float2 unpack_pair<__nv_bfloat16>(uint32_
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
 }
 
-// This thread's 64 keys (chunks c0 .. c0+7) of row t: reads dP (fp32, from
-// registers), P and dprobs (swizzled tiles); either accumulates sum P (dP + g)
-// into r_acc (dS == false) or writes dS = P (dP + g - r) to the dS tile.
-template <typename T, bool kDS>
-__device__ __forceinline__ void bwd_row_chunks(const float (&dp)[64], uint32_t sP, uint32_t sG, uint32_t sS, bool has_g,
-                                               int t, int c0, float r, float& r_acc) {
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint32_t pw[4], gw[4] = {0u, 0u, 0u, 0u};
-        ld_shared_v4(sw_chunk(sP, t, c0 + c), pw);
-        if (has_g) ld_shared_v4(sw_chunk(sG, t, c0 + c), gw);
-        uint32_t out[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float2 pp = unpack_pair<T>(pw[e]), gg = unpack_pair<T>(gw[e]);
-            const float d0 = dp[8 * c + 2 * e] + gg.x, d1 = dp[8 * c + 2 * e + 1] + gg.y;
-            if constexpr (kDS) {
-                out[e] = Pack<T>::two(pp.x * (d0 - r), pp.y * (d1 - r));
-            } else {
-                acc = fmaf(pp.x, d0, acc);
-                acc = fmaf(pp.y, d1, acc);
-            }
-        }
-        if constexpr (kDS) st_shared_v4(sw_chunk(sS, t, c0 + c), out[0], out[1], out[2], out[3]);
-    }
-    r_acc += acc;
-}
 
 // Rows [0, nvalid) of a [rows, X] slice into a ROWS-row swizzled tile whose
 // 64-column halves sit ROWS * 128 bytes apart (rows past nvalid zero-filled).
@@ -1248,8 +1198,8 @@ bwd_tc_rows_kernel(const BwdIO io) {
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sDO = smem_u32(smem + L::kOffDO), sRing = smem_u32(smem + L::kOffRing);
     float* stat = reinterpret_cast<float*>(smem + L::kOffStat);  // [2 warpgroups][128] partial row sums
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [0] dP and Bp done, [1] A done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
@@ -1258,10 +1208,11 @@ bwd_tc_rows_kernel(const BwdIO io) {
     const int nrows = min(128, io.Sq - r0);
     const int nsteps = (io.Skv + L::kKeys - 1) / L::kKeys;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t bar = smem_u32(&bars[0]);
+    const uint32_t bar_dp = smem_u32(&bars[0]), bar_a = smem_u32(&bars[1]);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_dp, 1);
+        mbar_init(bar_a, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1298,14 +1249,13 @@ bwd_tc_rows_kernel(const BwdIO io) {
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t idesc_dp = idesc_f16(128, 64, kBF16, false);
     constexpr uint32_t idesc_pk = idesc_f16(128, D, kBF16, true);
-    uint32_t phase = 0;
+    uint32_t phase_dp = 0, phase_a = 0;
     float r_acc = 0.f;
 
     for (int step = 0; step < nsteps; ++step) {
         const int st = step % L::kStages;
         const uint32_t sV = stage_v(st), sK = stage_k(st), sP = stage_p(st), sG = stage_g(st);
-        issue(step + 2);
-        asm volatile("cp.async.wait_group 2;" ::: "memory");
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's group (the next may be pending)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -1321,10 +1271,17 @@ bwd_tc_rows_kernel(const BwdIO io) {
             for (int kk = 0; kk < 4; ++kk)
                 tc_mma_f16(tmem + tB, sw128_desc(sP + kk * 32, 16, 1024), sw128_desc(sK + kk * 2048, 8192, 1024),
                            idesc_pk, (step > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(bar);
+            tc_commit(bar_dp);
         }
-        wait_bar(bar, phase, abort_flag, 8, 0);
-        phase ^= 1u;
+        // the previous step's A products were issued before this step's: once
+        // they are done its stage takes the loads two steps ahead
+        if (step > 0) {
+            wait_bar(bar_a, phase_a, abort_flag, 8, 1);
+            phase_a ^= 1u;
+        }
+        issue(step + 2);
+        wait_bar(bar_dp, phase_dp, abort_flag, 8, 0);
+        phase_dp ^= 1u;
         tc_fence_after();
         {
             // this warpgroup's 32 keys (chunks 4 wg .. 4 wg + 3) of row t
@@ -1366,12 +1323,11 @@ bwd_tc_rows_kernel(const BwdIO io) {
             for (int kk = 0; kk < 4; ++kk)
                 tc_mma_f16(tmem + tA, sw128_desc(sG + kk * 32, 16, 1024), sw128_desc(sK + kk * 2048, 8192, 1024),
                            idesc_pk, 1u);
-            tc_commit(bar);
+            tc_commit(bar_a);
         }
-        wait_bar(bar, phase, abort_flag, 8, 1);  // stage st and the dP columns are free again
-        phase ^= 1u;
-        tc_fence_after();
     }
+    wait_bar(bar_a, phase_a, abort_flag, 8, 2);
+    tc_fence_after();
     asm volatile("cp.async.wait_group 0;" ::: "memory");
 
     stat[wg * 128 + t] = r_acc;
@@ -1413,30 +1369,77 @@ bwd_tc_rows_kernel(const BwdIO io) {
     }
 }
 
+// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice into a swizzled
+// [64, 128] tile (two 64-key halves 8 KB apart; partial chunks zero-filled).
+template <typename T>
+__device__ __forceinline__ void load_ptile_q64_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
+    for (int u = threadIdx.x; u < 64 * 16; u += kBwdThreads) {
+        const int r = u >> 4, c = u & 15;
+        int bytes = (ncols - 8 * c) * 2;
+        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
+        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         dst + (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
+                     "l"(g), "r"(bytes)
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+    return v;
+}
+
+// Keys kernel layout: V_j once; a two-stage ring of 64-query steps (dO_i, Q_i
+// as [64, D] tiles, P_ij and dprobs_ij as [64, 128] tiles, the 64 row sums);
+// the dS^T tile [128 keys, 64 queries].
+template <int D>
+struct BwdKeysSmem {
+    static constexpr int kStages = 2;
+    static constexpr int kQ = 64;                 // queries per step
+    static constexpr int kQD = kQ * D * 2;        // [64, D] tile
+    static constexpr int kPG = kQ * 128 * 2;      // [64, 128] tile
+    static constexpr int kStage = 2 * kQD + 2 * kPG + 1024;
+    static constexpr int kOffV = 0;
+    static constexpr int kOffRing = 128 * D * 2;
+    static constexpr int kOffS = kOffRing + kStages * kStage;
+    static constexpr int kOffBar = kOffS + 128 * kQ * 2;
+    static constexpr int kSmem = kOffBar + 64 + 1024;
+    static_assert(kSmem <= 227 * 1024, "shared memory budget");
+};
+
+// CTA per 128-key tile of one key/value head; steps over the group's query
+// heads and 64-row query tiles.  Per step: dP^T = V_j dO_i^T (lanes = keys),
+// dV += P_ij^T dO_i (A read MN-major from the [query][key] tile),
+// dS^T = P^T * (dP^T + dprobs^T - r) written row-per-thread as a K-major tile,
+// dK += dS^T Q_i.  TMEM: dP^T [0, 64), dV [64, 64 + D), dK [64 + D, 64 + 2D).
 template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
 bwd_tc_keys_kernel(const BwdIO io) {
-    using L = BwdSmem<D>;
+    using L = BwdKeysSmem<D>;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
-    constexpr uint32_t kCols = 128 + 2 * D <= 256 ? 256 : 512;  // dP [0,128), dV [128,128+D), dK after
+    constexpr uint32_t kCols = 64 + 2 * D <= 256 ? 256 : 512;
+    constexpr uint32_t tDV = 64, tDK = 64 + D;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sV = smem_u32(smem + L::kOffA), sDO = smem_u32(smem + L::kOffB), sQ = smem_u32(smem + L::kOffC);
-    const uint32_t sP = smem_u32(smem + L::kOffP), sG = smem_u32(smem + L::kOffG), sS = smem_u32(smem + L::kOffS);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 1);
+    const uint32_t sV = smem_u32(smem + L::kOffV), sRing = smem_u32(smem + L::kOffRing);
+    const uint32_t sS = smem_u32(smem + L::kOffS);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [0] dP^T and dV done, [1] dK done
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
     const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const int j0 = kt * 128, ncols = min(128, io.Skv - j0);
-    const int nq = (io.Sq + 127) / 128;
+    const int nq = (io.Sq + L::kQ - 1) / L::kQ;
+    const int nsteps = io.group * nq;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t bar = smem_u32(&bars[0]);
-    const uint32_t tDV = 128, tDK = 128 + D;
+    const uint32_t bar_dp = smem_u32(&bars[0]), bar_k = smem_u32(&bars[1]);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar, 1);
+        mbar_init(bar_dp, 1);
+        mbar_init(bar_k, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -1444,78 +1447,125 @@ bwd_tc_keys_kernel(const BwdIO io) {
         tmem_alloc(smem_u32(tmem_slot), kCols);
         tmem_relinquish();
     }
+    auto st_do = [&](int st) { return sRing + st * L::kStage; };
+    auto st_q = [&](int st) { return sRing + st * L::kStage + L::kQD; };
+    auto st_p = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD; };
+    auto st_g = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD + L::kPG; };
+    auto st_r = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD + 2 * L::kPG; };
+    // one commit group per step (empty past the last step)
+    auto issue = [&](int step) {
+        if (step < nsteps) {
+            const int st = step % L::kStages;
+            const int h = hk * io.group + step / nq, r0 = (step % nq) * L::kQ, nrows = min(L::kQ, io.Sq - r0);
+            load_rows_sw128<T, 64>(st_do(st),
+                                   static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2,
+                                   io.sgo2, nrows, D);
+            load_rows_sw128<T, 64>(st_q(st),
+                                   static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2,
+                                   io.sq2, nrows, D);
+            load_ptile_q64_sw128<T>(
+                st_p(st), static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2 + j0, io.sp2,
+                nrows, ncols);
+            if (io.gp)
+                load_ptile_q64_sw128<T>(st_g(st),
+                                        static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 +
+                                            (long long)r0 * io.sgp2 + j0,
+                                        io.sgp2, nrows, ncols);
+            if (threadIdx.x < L::kQ) {  // row sums of the step's queries (4-byte copies)
+                const bool ok = (int)threadIdx.x < nrows;
+                const float* src = io.rowsum + ((long long)b * io.Hq + h) * io.Sq + r0 + (ok ? threadIdx.x : 0);
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(st_r(st) + 4 * threadIdx.x),
+                             "l"(src), "r"(ok ? 4 : 0)
+                             : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
     load_tile_sw128<T>(sV, static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1 + (long long)j0 * io.sv2, io.sv2,
-                       ncols, D);
+                       ncols, D);  // joins step 0's group
+    issue(0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    constexpr uint32_t idesc_dp = idesc_f16(128, 128, kBF16, false);
-    constexpr uint32_t idesc_kv = idesc_f16(128, D, kBF16, true) | (1u << 15);  // A MN-major too
-    uint32_t phase = 0;
-    int it = 0;
+    constexpr uint32_t idesc_dpt = idesc_f16(128, L::kQ, kBF16, false);
+    constexpr uint32_t idesc_dv = idesc_f16(128, D, kBF16, true) | (1u << 15);  // A MN-major too
+    constexpr uint32_t idesc_dk = idesc_f16(128, D, kBF16, true);
+    uint32_t phase_dp = 0, phase_k = 0;
+    const int key = t;  // this thread's TMEM lane and row of the dS^T tile
 
-    for (int g = 0; g < io.group; ++g) {
-        const int h = hk * io.group + g;
-        for (int i = 0; i < nq; ++i, ++it) {
-            const int r0 = i * 128, nrows = min(128, io.Sq - r0);
-            load_tile_sw128<T>(sDO, static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2,
-                               io.sgo2, nrows, D);
-            load_tile_sw128<T>(sQ, static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2,
-                               io.sq2, nrows, D);
-            load_ptile_sw128<T>(sP, static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2 + j0,
-                                io.sp2, nrows, ncols);
-            if (io.gp)
-                load_ptile_sw128<T>(sG,
-                                    static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 +
-                                        (long long)r0 * io.sgp2 + j0,
-                                    io.sgp2, nrows, ncols);
-            asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            if (threadIdx.x == 0) {
-                // dP = dO_i V_j^T (lanes = queries, columns = keys)
+    for (int step = 0; step < nsteps; ++step) {
+        const int st = step % L::kStages;
+        const uint32_t sDO = st_do(st), sQ = st_q(st), sP = st_p(st), sG = st_g(st);
+        const float* rs = reinterpret_cast<const float*>(smem + (st_r(st) - smem_u32(smem)));
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (threadIdx.x == 0) {
+            // dP^T = V_j dO_i^T (M = 128 keys, N = 64 queries, K = D)
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                    tc_mma_f16(tmem, sw128_desc(sDO + off, 16, 1024), sw128_desc(sV + off, 16, 1024), idesc_dp,
-                               kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk)
+                tc_mma_f16(tmem, sw128_desc(sV + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                           sw128_desc(sDO + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024), idesc_dpt, kk > 0 ? 1u : 0u);
+            // dV += P^T dO_i (M = 128 keys, N = D, K = 64 queries; both operands MN-major)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + tDV, sw128_desc(sP + kk * 2048, 8192, 1024), sw128_desc(sDO + kk * 2048, 8192, 1024),
+                           idesc_dv, (step > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_dp);
+        }
+        // dK of the previous step (issued before this step's products) frees
+        // the other stage and the dS^T tile
+        if (step > 0) {
+            wait_bar(bar_k, phase_k, abort_flag, 9, 1);
+            phase_k ^= 1u;
+        }
+        issue(step + 1);
+        wait_bar(bar_dp, phase_dp, abort_flag, 9, 0);
+        phase_dp ^= 1u;
+        tc_fence_after();
+        {
+            // queries [32 wg, 32 wg + 32) of key `key`
+            float dpt[32];
+            tmem_ld32(tmem + lane_base + wg * 32, dpt);
+            const uint32_t kcol = (key >> 6) * 8192 + (key & 7) * 2;
+            const uint32_t kchunk = (key & 63) >> 3;
+            uint32_t out[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                float ds[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int q = wg * 32 + e + u;
+                    const uint32_t off = kcol + q * 128 + ((kchunk ^ (q & 7)) << 4);
+                    const float pv = Pack<T>::load_bits(lds_u16(sP + off));
+                    const float gv = io.gp ? Pack<T>::load_bits(lds_u16(sG + off)) : 0.f;
+                    ds[u] = pv * (dpt[e + u] + gv - rs[q]);
                 }
-                // dV += P_i^T dO_i (lanes = keys): both operands MN-major, K = queries
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16(tmem + tDV, sw128_desc(sP + kk * 2048, 16384, 1024),
-                               sw128_desc(sDO + kk * 2048, 16384, 1024), idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar);
+                out[e / 2] = Pack<T>::two(ds[0], ds[1]);
             }
-            wait_bar(bar, phase, abort_flag, 9, 0);
-            phase ^= 1u;
-            tc_fence_after();
-            float dp[64];
-            tmem_ld32(tmem + lane_base + wg * 64, dp);
-            tmem_ld32(tmem + lane_base + wg * 64 + 32, dp + 32);
-            const float r = t < nrows ? io.rowsum[((long long)b * io.Hq + h) * io.Sq + r0 + t] : 0.f;
-            float unused = 0.f;
-            bwd_row_chunks<T, true>(dp, sP, sG, sS, io.gp != nullptr, t, wg * 8, r, unused);
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncthreads();
-            if (threadIdx.x == 0) {  // dK += dS_i^T Q_i
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_f16(tmem + tDK, sw128_desc(sS + kk * 2048, 16384, 1024),
-                               sw128_desc(sQ + kk * 2048, 16384, 1024), idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar);
-            }
-            wait_bar(bar, phase, abort_flag, 9, 1);
-            phase ^= 1u;
+            for (int c = 0; c < 4; ++c)
+                st_shared_v4(sS + key * 128 + (((4 * wg + c) ^ (key & 7)) << 4), out[4 * c], out[4 * c + 1],
+                             out[4 * c + 2], out[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (threadIdx.x == 0) {
             tc_fence_after();
-            __syncthreads();  // every read of this query tile's shared memory is done
+            // dK += dS^T Q_i (M = 128 keys, N = D, K = 64 queries)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                tc_mma_f16(tmem + tDK, sw128_desc(sS + kk * 32, 16, 1024), sw128_desc(sQ + kk * 2048, 8192, 1024),
+                           idesc_dk, (step > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_k);
         }
     }
+    wait_bar(bar_k, phase_k, abort_flag, 9, 2);
+    tc_fence_after();
 
     // dV (warpgroup 0) and dK (warpgroup 1) rows: lane t is key j0 + t
     {
@@ -1875,7 +1925,7 @@ cudaError_t launch_bwd_tc_t(const BwdProblem& p, cudaStream_t stream) {
     io.rowsum = p.rowsum;
     io.Hq = (int)p.Hq; io.group = (int)p.group; io.Sq = (int)p.Sq; io.Skv = (int)p.Skv;
     io.scale = p.scale;
-    constexpr int smem = BwdSmem<D>::kSmem, smem_rows = BwdRowsSmem<D>::kSmem;
+    constexpr int smem = BwdKeysSmem<D>::kSmem, smem_rows = BwdRowsSmem<D>::kSmem;
     auto kr = bwd_tc_rows_kernel<D, T>;
     auto kk = bwd_tc_keys_kernel<D, T>;
     cudaError_t e = prepare_kernel(kr, smem_rows, false);
