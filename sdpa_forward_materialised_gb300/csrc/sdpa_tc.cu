@@ -1187,9 +1187,16 @@ struct BwdRowsSmem {
 // product is accurate to about fp32 and the final subtraction loses nothing
 // beyond fp32 rounding.  TMEM: dP [0, 64), A = sum E K [64, 64 + D),
 // Bp = sum P K [64 + D, 64 + 2D).
+// Tensor-map order codes (see pick()) of the backward's TMA operands.
+struct BwdOrd {
+    uint32_t go, v, k, p, g;
+};
+
 template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-bwd_tc_rows_kernel(const BwdIO io) {
+bwd_tc_rows_kernel(const __grid_constant__ CUtensorMap tm_go, const __grid_constant__ CUtensorMap tm_v,
+                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_p,
+                   const __grid_constant__ CUtensorMap tm_g, const BwdIO io, const BwdOrd ord) {
     using L = BwdRowsSmem<D>;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kCols = 64 + 2 * D <= 256 ? 256 : 512;
@@ -1198,8 +1205,9 @@ bwd_tc_rows_kernel(const BwdIO io) {
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sDO = smem_u32(smem + L::kOffDO), sRing = smem_u32(smem + L::kOffRing);
     float* stat = reinterpret_cast<float*>(smem + L::kOffStat);  // [2 warpgroups][128] partial row sums
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [0] dP and Bp done, [1] A done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    // [0] dP and Bp done, [1] A done, [2 + stage] stage loaded
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 + L::kStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
@@ -1209,43 +1217,59 @@ bwd_tc_rows_kernel(const BwdIO io) {
     const int nsteps = (io.Skv + L::kKeys - 1) / L::kKeys;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t bar_dp = smem_u32(&bars[0]), bar_a = smem_u32(&bars[1]);
+    auto bar_full = [&](int st) { return smem_u32(&bars[2 + st]); };
+    const bool has_g = io.gp != nullptr;
 
     if (threadIdx.x == 0) {
         mbar_init(bar_dp, 1);
         mbar_init(bar_a, 1);
+        for (int st = 0; st < L::kStages; ++st) mbar_init(bar_full(st), 1);
         *abort_flag = 0;
         fence_mbar_init();
+        prefetch_tmap(&tm_go);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_p);
+        if (has_g) prefetch_tmap(&tm_g);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kCols);
         tmem_relinquish();
     }
-    const T* DO = static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2;
-    const T* Pr = static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2;
-    const T* Gr = io.gp ? static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 + (long long)r0 * io.sgp2 : nullptr;
-    const T* Vb = static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1;
-    const T* Kb = static_cast<const T*>(io.k) + b * io.sk0 + hk * io.sk1;
     auto stage_v = [&](int st) { return sRing + st * L::kStage; };
     auto stage_k = [&](int st) { return sRing + st * L::kStage + L::kKV; };
     auto stage_p = [&](int st) { return sRing + st * L::kStage + 2 * L::kKV; };
     auto stage_g = [&](int st) { return sRing + st * L::kStage + 2 * L::kKV + L::kPG; };
-    // one commit group per step (empty past the last step)
+    // TMA loads of one step into its stage (thread 0; out-of-range rows and
+    // keys arrive as zeros); step 0 also brings the dO tile
     auto issue = [&](int step) {
-        if (step < nsteps) {
-            const int st = step % L::kStages, j0 = step * L::kKeys, nk = min(L::kKeys, io.Skv - j0);
-            load_rows_sw128<T, 64>(stage_v(st), Vb + (long long)j0 * io.sv2, io.sv2, nk, D);
-            load_rows_sw128<T, 64>(stage_k(st), Kb + (long long)j0 * io.sk2, io.sk2, nk, D);
-            load_ptile64_sw128<T>(stage_p(st), Pr + j0, io.sp2, nrows, nk);
-            if (Gr) load_ptile64_sw128<T>(stage_g(st), Gr + j0, io.sgp2, nrows, nk);
+        if (step >= nsteps) return;
+        const int st = step % L::kStages, j0 = step * L::kKeys;
+        const uint32_t full = bar_full(st);
+        mbar_arrive_expect_tx(full, 2 * L::kKV + (has_g ? 2 : 1) * L::kPG + (step == 0 ? 128 * D * 2 : 0));
+        if (step == 0)
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d(sDO + c * 16384, &tm_go, full, c * 64, pick(ord.go & 3, r0, h, b),
+                            pick((ord.go >> 2) & 3, r0, h, b), pick((ord.go >> 4) & 3, r0, h, b));
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(stage_v(st) + c * 8192, &tm_v, full, c * 64, pick(ord.v & 3, j0, hk, b),
+                        pick((ord.v >> 2) & 3, j0, hk, b), pick((ord.v >> 4) & 3, j0, hk, b));
+            tma_load_4d(stage_k(st) + c * 8192, &tm_k, full, c * 64, pick(ord.k & 3, j0, hk, b),
+                        pick((ord.k >> 2) & 3, j0, hk, b), pick((ord.k >> 4) & 3, j0, hk, b));
         }
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        tma_load_4d(stage_p(st), &tm_p, full, j0, pick(ord.p & 3, r0, h, b), pick((ord.p >> 2) & 3, r0, h, b),
+                    pick((ord.p >> 4) & 3, r0, h, b));
+        if (has_g)
+            tma_load_4d(stage_g(st), &tm_g, full, j0, pick(ord.g & 3, r0, h, b), pick((ord.g >> 2) & 3, r0, h, b),
+                        pick((ord.g >> 4) & 3, r0, h, b));
     };
-    load_tile_sw128<T>(sDO, DO, io.sgo2, nrows, D);  // joins step 0's group
-    issue(0);
-    issue(1);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barriers initialised
     tc_fence_after();
+    if (threadIdx.x == 0) {
+        issue(0);
+        issue(1);
+    }
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t idesc_dp = idesc_f16(128, 64, kBF16, false);
     constexpr uint32_t idesc_pk = idesc_f16(128, D, kBF16, true);
@@ -1255,10 +1279,7 @@ bwd_tc_rows_kernel(const BwdIO io) {
     for (int step = 0; step < nsteps; ++step) {
         const int st = step % L::kStages;
         const uint32_t sV = stage_v(st), sK = stage_k(st), sP = stage_p(st), sG = stage_g(st);
-        asm volatile("cp.async.wait_group 1;" ::: "memory");  // this step's group (the next may be pending)
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
+        wait_bar(bar_full(st), (step / L::kStages) & 1, abort_flag, 8, 3);
         tc_fence_after();
         if (threadIdx.x == 0) {
             // dP = dO V_j^T (N = 64 keys)
@@ -1279,7 +1300,7 @@ bwd_tc_rows_kernel(const BwdIO io) {
             wait_bar(bar_a, phase_a, abort_flag, 8, 1);
             phase_a ^= 1u;
         }
-        issue(step + 2);
+        if (threadIdx.x == 0) issue(step + 2);
         wait_bar(bar_dp, phase_dp, abort_flag, 8, 0);
         phase_dp ^= 1u;
         tc_fence_after();
@@ -1293,7 +1314,7 @@ bwd_tc_rows_kernel(const BwdIO io) {
                 const uint32_t ap = sw_chunk(sP, t, 4 * wg + c), ag = sw_chunk(sG, t, 4 * wg + c);
                 uint32_t pw[4], gw[4] = {0u, 0u, 0u, 0u};
                 ld_shared_v4(ap, pw);
-                if (Gr) ld_shared_v4(ag, gw);
+                if (has_g) ld_shared_v4(ag, gw);
                 uint32_t hi[4], lo[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -1328,7 +1349,6 @@ bwd_tc_rows_kernel(const BwdIO io) {
     }
     wait_bar(bar_a, phase_a, abort_flag, 8, 2);
     tc_fence_after();
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
 
     stat[wg * 128 + t] = r_acc;
     __syncthreads();
@@ -1931,7 +1951,22 @@ cudaError_t launch_bwd_tc_t(const BwdProblem& p, cudaStream_t stream) {
     cudaError_t e = prepare_kernel(kr, smem_rows, false);
     if (e != cudaSuccess) return e;
     if ((e = prepare_kernel(kk, smem, false)) != cudaSuccess) return e;
-    kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem_rows, stream>>>(io);
+    // tensor maps of the rows kernel's TMA operands ([B, H, S, X], 64-wide boxes)
+    CUtensorMap mgo, mv, mk, mp, mg;
+    BwdOrd ord;
+    std::memset(&ord, 0, sizeof(ord));
+    if (!make_map(&mgo, p.dtype, p.dout, p.Dv, p.Sq, p.Hq, p.B, p.sgo, 128, &ord.go) ||
+        !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 64, &ord.v) ||
+        !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, 64, &ord.k) ||
+        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 128, &ord.p))
+        return cudaErrorNotSupported;
+    if (p.dprobs) {
+        if (!make_map(&mg, p.dtype, p.dprobs, p.Skv, p.Sq, p.Hq, p.B, p.sgp, 128, &ord.g)) return cudaErrorNotSupported;
+    } else {
+        mg = mp;  // never read
+    }
+    kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem_rows, stream>>>(
+        mgo, mv, mk, mp, mg, io, ord);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     kk<<<dim3((unsigned)((p.Skv + 127) / 128), (unsigned)p.Hkv, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
     return cudaGetLastError();
