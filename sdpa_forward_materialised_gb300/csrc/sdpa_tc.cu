@@ -1189,7 +1189,7 @@ struct BwdRowsSmem {
 // Bp = sum P K [64 + D, 64 + 2D).
 // Tensor-map order codes (see pick()) of the backward's TMA operands.
 struct BwdOrd {
-    uint32_t go, v, k, p, g;
+    uint32_t go, v, k, q, p, g;
 };
 
 template <int D, typename T>
@@ -1436,7 +1436,9 @@ struct BwdKeysSmem {
 // dK += dS^T Q_i.  TMEM: dP^T [0, 64), dV [64, 64 + D), dK [64 + D, 64 + 2D).
 template <int D, typename T>
 __global__ void __launch_bounds__(kBwdThreads, 1)
-bwd_tc_keys_kernel(const BwdIO io) {
+bwd_tc_keys_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_go,
+                   const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_p,
+                   const __grid_constant__ CUtensorMap tm_g, const BwdIO io, const BwdOrd ord) {
     using L = BwdKeysSmem<D>;
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
     constexpr uint32_t kCols = 64 + 2 * D <= 256 ? 256 : 512;
@@ -1445,8 +1447,9 @@ bwd_tc_keys_kernel(const BwdIO io) {
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sV = smem_u32(smem + L::kOffV), sRing = smem_u32(smem + L::kOffRing);
     const uint32_t sS = smem_u32(smem + L::kOffS);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);  // [0] dP^T and dV done, [1] dK done
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
+    // [0] dP^T and dV done, [1] dK done, [2 + stage] stage loaded
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 + L::kStages);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, wg = threadIdx.x / 128, t = threadIdx.x % 128;
@@ -1457,11 +1460,19 @@ bwd_tc_keys_kernel(const BwdIO io) {
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t bar_dp = smem_u32(&bars[0]), bar_k = smem_u32(&bars[1]);
 
+    auto bar_full = [&](int st) { return smem_u32(&bars[2 + st]); };
+    const bool has_g = io.gp != nullptr;
     if (threadIdx.x == 0) {
         mbar_init(bar_dp, 1);
         mbar_init(bar_k, 1);
+        for (int st = 0; st < L::kStages; ++st) mbar_init(bar_full(st), 1);
         *abort_flag = 0;
         fence_mbar_init();
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_go);
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_p);
+        if (has_g) prefetch_tmap(&tm_g);
     }
     if (warp == 0) {
         tmem_alloc(smem_u32(tmem_slot), kCols);
@@ -1472,41 +1483,50 @@ bwd_tc_keys_kernel(const BwdIO io) {
     auto st_p = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD; };
     auto st_g = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD + L::kPG; };
     auto st_r = [&](int st) { return sRing + st * L::kStage + 2 * L::kQD + 2 * L::kPG; };
-    // one commit group per step (empty past the last step)
-    auto issue = [&](int step) {
-        if (step < nsteps) {
+    // TMA loads of one step into its stage (thread 0; out-of-range rows and
+    // keys arrive as zeros); step 0 also brings the V tile
+    auto issue_tma = [&](int step) {
+        if (step >= nsteps) return;
+        const int st = step % L::kStages;
+        const int h = hk * io.group + step / nq, r0 = (step % nq) * L::kQ;
+        const uint32_t full = bar_full(st);
+        mbar_arrive_expect_tx(full, 2 * L::kQD + (has_g ? 2 : 1) * L::kPG + (step == 0 ? 128 * D * 2 : 0));
+        if (step == 0)
+            for (int c = 0; c < D / 64; ++c)
+                tma_load_4d(sV + c * 16384, &tm_v, full, c * 64, pick(ord.v & 3, j0, hk, b),
+                            pick((ord.v >> 2) & 3, j0, hk, b), pick((ord.v >> 4) & 3, j0, hk, b));
+        for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(st_do(st) + c * 8192, &tm_go, full, c * 64, pick(ord.go & 3, r0, h, b),
+                        pick((ord.go >> 2) & 3, r0, h, b), pick((ord.go >> 4) & 3, r0, h, b));
+            tma_load_4d(st_q(st) + c * 8192, &tm_q, full, c * 64, pick(ord.q & 3, r0, h, b),
+                        pick((ord.q >> 2) & 3, r0, h, b), pick((ord.q >> 4) & 3, r0, h, b));
+        }
+        for (int c = 0; c < 2; ++c) {  // the two 64-key halves
+            tma_load_4d(st_p(st) + c * 8192, &tm_p, full, j0 + 64 * c, pick(ord.p & 3, r0, h, b),
+                        pick((ord.p >> 2) & 3, r0, h, b), pick((ord.p >> 4) & 3, r0, h, b));
+            if (has_g)
+                tma_load_4d(st_g(st) + c * 8192, &tm_g, full, j0 + 64 * c, pick(ord.g & 3, r0, h, b),
+                            pick((ord.g >> 2) & 3, r0, h, b), pick((ord.g >> 4) & 3, r0, h, b));
+        }
+    };
+    // row sums of a step's queries: 4-byte copies, one commit group per step
+    auto issue_r = [&](int step) {
+        if (step < nsteps && threadIdx.x < L::kQ) {
             const int st = step % L::kStages;
             const int h = hk * io.group + step / nq, r0 = (step % nq) * L::kQ, nrows = min(L::kQ, io.Sq - r0);
-            load_rows_sw128<T, 64>(st_do(st),
-                                   static_cast<const T*>(io.go) + b * io.sgo0 + h * io.sgo1 + (long long)r0 * io.sgo2,
-                                   io.sgo2, nrows, D);
-            load_rows_sw128<T, 64>(st_q(st),
-                                   static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2,
-                                   io.sq2, nrows, D);
-            load_ptile_q64_sw128<T>(
-                st_p(st), static_cast<const T*>(io.p) + b * io.sp0 + h * io.sp1 + (long long)r0 * io.sp2 + j0, io.sp2,
-                nrows, ncols);
-            if (io.gp)
-                load_ptile_q64_sw128<T>(st_g(st),
-                                        static_cast<const T*>(io.gp) + b * io.sgp0 + h * io.sgp1 +
-                                            (long long)r0 * io.sgp2 + j0,
-                                        io.sgp2, nrows, ncols);
-            if (threadIdx.x < L::kQ) {  // row sums of the step's queries (4-byte copies)
-                const bool ok = (int)threadIdx.x < nrows;
-                const float* src = io.rowsum + ((long long)b * io.Hq + h) * io.Sq + r0 + (ok ? threadIdx.x : 0);
-                asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(st_r(st) + 4 * threadIdx.x),
-                             "l"(src), "r"(ok ? 4 : 0)
-                             : "memory");
-            }
+            const bool ok = (int)threadIdx.x < nrows;
+            const float* src = io.rowsum + ((long long)b * io.Hq + h) * io.Sq + r0 + (ok ? threadIdx.x : 0);
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(st_r(st) + 4 * threadIdx.x), "l"(src),
+                         "r"(ok ? 4 : 0)
+                         : "memory");
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    load_tile_sw128<T>(sV, static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1 + (long long)j0 * io.sv2, io.sv2,
-                       ncols, D);  // joins step 0's group
-    issue(0);
     tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // barriers initialised
     tc_fence_after();
+    if (threadIdx.x == 0) issue_tma(0);
+    issue_r(0);
     const uint32_t tmem = *tmem_slot;
     constexpr uint32_t idesc_dpt = idesc_f16(128, L::kQ, kBF16, false);
     constexpr uint32_t idesc_dv = idesc_f16(128, D, kBF16, true) | (1u << 15);  // A MN-major too
@@ -1518,8 +1538,8 @@ bwd_tc_keys_kernel(const BwdIO io) {
         const int st = step % L::kStages;
         const uint32_t sDO = st_do(st), sQ = st_q(st), sP = st_p(st), sG = st_g(st);
         const float* rs = reinterpret_cast<const float*>(smem + (st_r(st) - smem_u32(smem)));
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        fence_proxy_async_smem();
+        asm volatile("cp.async.wait_group 0;" ::: "memory");  // this step's row sums
+        wait_bar(bar_full(st), (step / L::kStages) & 1, abort_flag, 9, 3);
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
@@ -1542,7 +1562,8 @@ bwd_tc_keys_kernel(const BwdIO io) {
             wait_bar(bar_k, phase_k, abort_flag, 9, 1);
             phase_k ^= 1u;
         }
-        issue(step + 1);
+        if (threadIdx.x == 0) issue_tma(step + 1);
+        issue_r(step + 1);
         wait_bar(bar_dp, phase_dp, abort_flag, 9, 0);
         phase_dp ^= 1u;
         tc_fence_after();
@@ -1561,7 +1582,7 @@ bwd_tc_keys_kernel(const BwdIO io) {
                     const int q = wg * 32 + e + u;
                     const uint32_t off = kcol + q * 128 + ((kchunk ^ (q & 7)) << 4);
                     const float pv = Pack<T>::load_bits(lds_u16(sP + off));
-                    const float gv = io.gp ? Pack<T>::load_bits(lds_u16(sG + off)) : 0.f;
+                    const float gv = has_g ? Pack<T>::load_bits(lds_u16(sG + off)) : 0.f;
                     ds[u] = pv * (dpt[e + u] + gv - rs[q]);
                 }
                 out[e / 2] = Pack<T>::two(ds[0], ds[1]);
@@ -1968,7 +1989,21 @@ cudaError_t launch_bwd_tc_t(const BwdProblem& p, cudaStream_t stream) {
     kr<<<dim3((unsigned)((p.Sq + 127) / 128), (unsigned)p.Hq, (unsigned)p.B), kBwdThreads, smem_rows, stream>>>(
         mgo, mv, mk, mp, mg, io, ord);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    kk<<<dim3((unsigned)((p.Skv + 127) / 128), (unsigned)p.Hkv, (unsigned)p.B), kBwdThreads, smem, stream>>>(io);
+    CUtensorMap kv, kgo, kq, kp, kg;
+    BwdOrd ko;
+    std::memset(&ko, 0, sizeof(ko));
+    if (!make_map(&kv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 128, &ko.v) ||
+        !make_map(&kgo, p.dtype, p.dout, p.Dv, p.Sq, p.Hq, p.B, p.sgo, 64, &ko.go) ||
+        !make_map(&kq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, 64, &ko.q) ||
+        !make_map(&kp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 64, &ko.p))
+        return cudaErrorNotSupported;
+    if (p.dprobs) {
+        if (!make_map(&kg, p.dtype, p.dprobs, p.Skv, p.Sq, p.Hq, p.B, p.sgp, 64, &ko.g)) return cudaErrorNotSupported;
+    } else {
+        kg = kp;  // never read
+    }
+    kk<<<dim3((unsigned)((p.Skv + 127) / 128), (unsigned)p.Hkv, (unsigned)p.B), kBwdThreads, smem, stream>>>(
+        kv, kgo, kq, kp, kg, io, ko);
     return cudaGetLastError();
 }
 }  // namespace
