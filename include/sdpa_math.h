@@ -84,8 +84,10 @@ typedef enum {
     SDPA_VARIANT_TC_FUSED = 3,   /* tcgen05: one sweep, the whole score row block kept in TMEM */
     SDPA_VARIANT_DECODE = 4,     /* few query rows per KV head: KV split across a CTA cluster */
     SDPA_VARIANT_TC_PAIRED = 5,  /* TC_TWOPASS with two query tiles per CTA sharing each K/V load */
-    SDPA_VARIANT_SPLIT = 6       /* few query rows, long key sequence: keys split over a cluster of up
+    SDPA_VARIANT_SPLIT = 6,      /* few query rows, long key sequence: keys split over a cluster of up
                                     to 16 CTAs, scores kept on chip, V streamed (split-KV) */
+    SDPA_VARIANT_TC_DECODE = 7   /* few query rows, D = Dv = 128, f16/bf16: the cluster split of SPLIT
+                                    with S^T = K Q^T and O^T = V^T P^T on the tensor cores, K / V by TMA */
 } sdpa_variant;
 
 typedef struct {

@@ -32,7 +32,7 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED
           3: "SDPA_ERR_CUDA", 4: "SDPA_ERR_TIMEOUT"}
 SDPA_F32, SDPA_F16, SDPA_BF16, SDPA_BOOL = range(4)
 MASK_NONE, MASK_BOOL, MASK_ADDITIVE = range(3)
-VARIANTS = {"auto": 0, "simt": 1, "twopass": 2, "fused": 3, "decode": 4, "paired": 5, "split": 6}
+VARIANTS = {"auto": 0, "simt": 1, "twopass": 2, "fused": 3, "decode": 4, "paired": 5, "split": 6, "tcdecode": 7}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 

@@ -73,6 +73,8 @@ int tc_query_tiles(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 bool split_supports(const Problem& p, const char** why);
+bool tc_decode_supports(const Problem& p, const char** why);
+cudaError_t launch_tc_decode(const Problem& p, cudaStream_t stream);
 cudaError_t launch_split(const Problem& p, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdProblem& p, cudaStream_t stream);   // CUDA-core kernels, any shape
 bool bwd_tc_supports(const BwdProblem& p, const char** why);

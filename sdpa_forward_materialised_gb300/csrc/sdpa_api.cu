@@ -31,7 +31,7 @@ sdpa_status fail(sdpa_status s, const char* fmt, ...) {
     return s;
 }
 
-// SDPA_MATH_VARIANT=auto|simt|twopass|paired|fused|decode|split, read once at load.
+// SDPA_MATH_VARIANT=auto|simt|twopass|paired|fused|decode|split|tcdecode, read once at load.
 sdpa_variant env_variant() {
     static const sdpa_variant v = [] {
         const char* e = std::getenv("SDPA_MATH_VARIANT");
@@ -42,6 +42,7 @@ sdpa_variant env_variant() {
         if (!std::strcmp(e, "fused")) return SDPA_VARIANT_TC_FUSED;
         if (!std::strcmp(e, "decode")) return SDPA_VARIANT_DECODE;
         if (!std::strcmp(e, "split")) return SDPA_VARIANT_SPLIT;
+        if (!std::strcmp(e, "tcdecode")) return SDPA_VARIANT_TC_DECODE;
         return SDPA_VARIANT_AUTO;
     }();
     return v;
@@ -202,6 +203,7 @@ sdpa_variant choose(const sdpa::Problem& p) {
     const char* why = nullptr;
     if (p.dtype == SDPA_F32) return SDPA_VARIANT_SIMT;
     if (sdpa::decode_supports(p, &why)) return SDPA_VARIANT_DECODE;
+    if (sdpa::tc_decode_supports(p, &why)) return SDPA_VARIANT_TC_DECODE;
     if (sdpa::split_supports(p, &why)) return SDPA_VARIANT_SPLIT;
     if (p.Skv <= kFusedMaxKeys && sdpa::tc_supports(p, true, &why)) return SDPA_VARIANT_TC_FUSED;
     if (sdpa::tc_supports(p, false, &why))
@@ -230,6 +232,11 @@ sdpa_status resolve(const sdpa::Problem& p, sdpa_variant requested, sdpa_variant
         case SDPA_VARIANT_SPLIT:
             if (!sdpa::split_supports(p, &why))
                 return fail(SDPA_ERR_UNSUPPORTED, "split variant cannot serve this call: %s", why);
+            *out = v;
+            return SDPA_OK;
+        case SDPA_VARIANT_TC_DECODE:
+            if (!sdpa::tc_decode_supports(p, &why))
+                return fail(SDPA_ERR_UNSUPPORTED, "tensor-core decode variant cannot serve this call: %s", why);
             *out = v;
             return SDPA_OK;
         default:
@@ -285,6 +292,7 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
         case SDPA_VARIANT_TC_FUSED: e = sdpa::launch_tc(p, 3, st); break;
         case SDPA_VARIANT_DECODE: e = sdpa::launch_decode(p, st); break;
         case SDPA_VARIANT_SPLIT: e = sdpa::launch_split(p, st); break;
+        case SDPA_VARIANT_TC_DECODE: e = sdpa::launch_tc_decode(p, st); break;
         default: e = sdpa::launch_simt(p, st); break;
     }
     // A tensor-core family refuses (before launching anything) when the

@@ -130,6 +130,14 @@ template <> struct Pack<__nv_bfloat16> {
     }
 };
 
+template <typename T> __device__ __forceinline__ T from_float(float x);
+template <> __device__ __forceinline__ __half from_float<__half>(float x) { return __float2half_rn(x); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ uint16_t bits16(__half x) { return __half_as_ushort(x); }
+__device__ __forceinline__ uint16_t bits16(__nv_bfloat16 x) { return __bfloat16_as_ushort(x); }
+
 // Base-2 additive term of a user mask at (row, key): 0 / -inf for a bool
 // mask, mask*log2(e) for an additive one.  Row and key must be in range.
 template <typename T>
@@ -1072,6 +1080,295 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
 }
 
 
+// ---------------------------------------------------------------- tensor-core decode / split-KV
+//
+// Few query rows per key/value head (R = group * Sq <= 16), any number of keys,
+// D = Dv = 128.  One cluster of C CTAs per (batch, key/value head); CTA c owns
+// a contiguous chunk of keys, walked in 128-key tiles.  The dot products run
+// on the tensor cores with the keys on the TMEM lanes:
+//   sweep 1: S^T = K_tile Q^T (M = 128 keys, N = 16 query rows, zero-padded),
+//     so thread t reads key t's R scores with one tcgen05.ld; the scores of the
+//     chunk stay in shared memory;
+//   the chunk statistics are merged over the cluster through DSMEM (every CTA
+//     forms the same lse per row);
+//   sweep 2: P = exp2(s - lse) per (row, key), stored to global memory and as
+//     the B operand of O^T += V_tile^T P^T (M = 128 value columns, A read
+//     MN-major from the V tile as loaded);
+//   the partial O^T is summed over the cluster by column slices.
+// K and V tiles arrive by TMA through one ring shared by both sweeps.
+
+struct TcDecParams {
+    const void* q; long long sq0, sq1, sq2;
+    const void* mask; int mask_kind, mask_dtype; long long sm0, sm1, sm2;
+    void* o; long long so0, so1, so2;
+    void* p; long long sp0, sp1, sp2;
+    float* lse;
+    int Hq, Sq, Skv, group, rows, chunk, causal, stages;
+    float c2;  // scale * log2(e)
+    uint32_t ord_k, ord_v;
+    int off_ss, off_part, off_st;  // dynamic shared-memory layout after the fixed part
+};
+
+constexpr int kDecThreads = 128;
+constexpr int kDecMaxCluster = 16;
+constexpr int kDecSmemMax = 220 * 1024;  // dynamic shared memory (the kernel also has a little static)
+struct DecLayout {
+    static constexpr int kTile = 128 * 128 * 2;         // one K or V tile
+    static constexpr int kMaxStages = 3;
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffQ = kMaxStages * kTile;     // [16 rows, 128] K-major
+    static constexpr int kOffP = kOffQ + 4096;           // two [16 rows, 128 keys] P^T operands
+    static constexpr int kOffBar = kOffP + 8192;
+    static constexpr int kFixed = kOffBar + 128;
+    // the ring is placed for kMaxStages; a two-stage launch moves everything after it down
+    static constexpr int kRingShrink2 = kTile;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kDecThreads, 1)
+tc_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                 const TcDecParams p) {
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    constexpr uint32_t kCols = 64;  // S^T [0, 32) double-buffered, O^T [32, 48)
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ float lse_s[16];
+    __shared__ int row_h[16], row_i[16];
+    const int shrink = p.stages == 2 ? DecLayout::kRingShrink2 : 0;
+    const uint32_t sRing = smem_u32(smem);
+    const uint32_t sQ = smem_u32(smem + DecLayout::kOffQ - shrink), sP = smem_u32(smem + DecLayout::kOffP - shrink);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + DecLayout::kOffBar - shrink);  // full[3], s[2], o
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* ss = reinterpret_cast<float*>(smem + p.off_ss);      // [R][chunk] scores, base-2 units
+    float* part = reinterpret_cast<float*>(smem + p.off_part);  // [R][128] partial O
+    float* st = reinterpret_cast<float*>(smem + p.off_st);      // [R][2] chunk (max, sum)
+    auto bar_full = [&](int s) { return smem_u32(&bars[s]); };
+    auto bar_s = [&](int i) { return smem_u32(&bars[3 + (i & 1)]); };
+    const uint32_t bar_o = smem_u32(&bars[5]);
+
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    const uint32_t crank = cluster_ctarank();
+    const int C = (int)gridDim.x;
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int k0 = (int)crank * p.chunk;
+    const int n = max(0, min(p.Skv, k0 + p.chunk) - k0);
+    const int nt = (n + 127) / 128;
+    const int R = p.rows, S = p.stages;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+    if (t == 0) {
+        for (int i = 0; i < 6; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(smem_u32(tmem_slot), kCols);
+        tmem_relinquish();
+    }
+    // Q rows (zero rows past R) in the swizzled K-major layout; P^T operands zeroed
+    for (int u = t; u < 16 * 16; u += kDecThreads) {
+        const int r = u / 16, c = u % 16;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (r < R) {
+            const T* qr = static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
+                          (long long)(r % p.Sq) * p.sq2;
+            v = *reinterpret_cast<const uint4*>(qr + c * 8);
+        }
+        st_shared_v4(sQ + (c >> 3) * 2048 + r * 128 + (((c & 7) ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+    }
+    for (int u = t; u < 8192 / 16; u += kDecThreads) st_shared_v4(sP + 16 * u, 0u, 0u, 0u, 0u);
+    if (t < R) {
+        row_h[t] = hk * p.group + t / p.Sq;
+        row_i[t] = t % p.Sq;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // ring uses: K tiles 0 .. nt-1, then V tiles 0 .. nt-1 (thread 0 issues)
+    auto issue = [&](int use) {
+        if (use >= 2 * nt) return;
+        const bool is_v = use >= nt;
+        const int i = is_v ? use - nt : use, row0 = k0 + i * 128;
+        const int slot = use % S;
+        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
+        const uint32_t ord = is_v ? p.ord_v : p.ord_k;
+        mbar_arrive_expect_tx(bar_full(slot), DecLayout::kTile);
+        for (int c = 0; c < 2; ++c)
+            tma_load_4d(sRing + slot * DecLayout::kTile + c * 16384, tm, bar_full(slot), c * 64,
+                        pick(ord & 3, row0, hk, b), pick((ord >> 2) & 3, row0, hk, b), pick((ord >> 4) & 3, row0, hk, b));
+    };
+    if (t == 0)
+        for (int u = 0; u < S; ++u) issue(u);
+    constexpr uint32_t idesc_s = idesc_f16(128, 16, kBF16, false);
+    constexpr uint32_t idesc_o = idesc_f16(128, 16, kBF16, false) | (1u << 15);  // A (V^T) MN-major
+
+    // ---- sweep 1: scores
+    for (int i = 0; i < nt; ++i) {
+        const int slot = i % S;
+        const uint32_t sK = sRing + slot * DecLayout::kTile;
+        if (t == 0) {
+            wait_bar(bar_full(slot), (i / S) & 1, abort_flag, 10, 0);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_f16(tmem + (i & 1) * 16, sw128_desc(sK + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024),
+                           sw128_desc(sQ + (kk / 4) * 2048 + (kk % 4) * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+            tc_commit(bar_s(i));
+        }
+        wait_bar(bar_s(i), (i >> 1) & 1, abort_flag, 10, 1);
+        tc_fence_after();
+        float acc[16];
+        tmem_ld16(tmem + lane_base + (i & 1) * 16, acc);
+        const int j = i * 128 + t, key = k0 + j;
+        if (j < n) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                if (r < R) {
+                    float sc = __fmul_rn(acc[r], p.c2);
+                    if (p.causal && key > row_i[r]) sc = -CUDART_INF_F;
+                    if (p.mask_kind != kMaskNone) {
+                        const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + key;
+                        if (p.mask_kind == kMaskBool) {
+                            if (static_cast<const unsigned char*>(p.mask)[off] == 0) sc = -CUDART_INF_F;
+                        } else {
+                            const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                                 : Pack<T>::load(static_cast<const T*>(p.mask) + off);
+                            sc = __fmaf_rn(m, kLog2e, sc);
+                        }
+                    }
+                    ss[r * p.chunk + j] = sc;
+                }
+        }
+        tc_fence_before();
+        __syncthreads();  // S^T buffer and the K tile consumed
+        if (t == 0) issue(i + S);
+    }
+
+    // per-row (max, sum of exp2) of the chunk: one warp per row
+    for (int r = warp; r < R; r += kDecThreads / 32) {
+        float m = -CUDART_INF_F;
+        for (int j = lane; j < n; j += 32) m = fmaxf(m, ss[r * p.chunk + j]);
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        if (m != -CUDART_INF_F)
+            for (int j = lane; j < n; j += 32) l += exp2f(ss[r * p.chunk + j] - m);
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            st[2 * r] = m;
+            st[2 * r + 1] = l;
+        }
+    }
+    // ---- the cluster's statistics -> the same lse in every CTA
+    cluster_barrier();
+    if (t < R) {
+        float mc[kDecMaxCluster], lc[kDecMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kDecMaxCluster; ++c)
+            if (c < C) {
+                mc[c] = ld_cluster_f32(&st[2 * t], (uint32_t)c);
+                lc[c] = ld_cluster_f32(&st[2 * t + 1], (uint32_t)c);
+            }
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < kDecMaxCluster; ++c)
+            if (c < C) m = fmaxf(m, mc[c]);
+        float l = 0.f;
+        if (m != -CUDART_INF_F) {
+#pragma unroll
+            for (int c = 0; c < kDecMaxCluster; ++c)
+                if (c < C && mc[c] != -CUDART_INF_F) l += lc[c] * exp2f(mc[c] - m);
+        }
+        lse_s[t] = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
+    }
+    __syncthreads();
+
+    // ---- sweep 2: P (stored, and as the rounded B operand), O^T += V^T P^T
+    for (int i = 0; i < nt; ++i) {
+        const int use = nt + i, slot = use % S;
+        const uint32_t sV = sRing + slot * DecLayout::kTile, sPb = sP + (i & 1) * 4096;
+        const int j = i * 128 + t;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (r < R) {
+                const float L = lse_s[r];
+                const float pr = (j < n && L != -CUDART_INF_F) ? exp2f(ss[r * p.chunk + j] - L) : 0.f;
+                const T pt = from_float<T>(pr);
+                if (j < n) {
+                    T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
+                    prow[k0 + j] = pt;
+                }
+                asm volatile("st.shared.b16 [%0], %1;" ::"r"(sPb + (t >> 6) * 2048 + r * 128 +
+                                                             ((((t & 63) >> 3) ^ (r & 7)) << 4) + (t & 7) * 2),
+                             "h"(bits16(pt))
+                             : "memory");
+            }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (t == 0) {
+            tc_fence_after();
+            wait_bar(bar_full(slot), (use / S) & 1, abort_flag, 10, 2);
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_f16(tmem + 32, sw128_desc(sV + kk * 2048, 16384, 1024),
+                           sw128_desc(sPb + (kk / 4) * 2048 + (kk % 4) * 32, 16, 1024), idesc_o,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(bar_o);
+            wait_bar(bar_o, i & 1, abort_flag, 10, 3);  // the V tile and this P^T buffer are free again
+            issue(use + S);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- partial O (lane t = value column t), then the cluster sum by column slices
+    {
+        float o[16];
+        tmem_ld16(tmem + lane_base + 32, o);
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (r < R) part[r * 128 + t] = nt > 0 ? o[r] : 0.f;
+    }
+    cluster_barrier();
+    const int cols = (128 + C - 1) / C;
+    const int c0 = (int)crank * cols, c1 = min(128, c0 + cols);
+    for (int e = t; e < R * max(0, c1 - c0); e += kDecThreads) {
+        const int r = e / (c1 - c0), d = c0 + e % (c1 - c0);
+        float pc[kDecMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kDecMaxCluster; ++c)
+            if (c < C) pc[c] = ld_cluster_f32(&part[r * 128 + d], (uint32_t)c);
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kDecMaxCluster; ++c)
+            if (c < C) acc += pc[c];
+        const bool dead = lse_s[r] == -CUDART_INF_F;
+        T* orow = static_cast<T*>(p.o) + b * p.so0 + row_h[r] * p.so1 + (long long)row_i[r] * p.so2;
+        orow[d] = from_float<T>(dead ? 0.f : acc);
+    }
+    if (crank == 0 && p.lse && t < R) {
+        const float L = lse_s[t];
+        p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
+    }
+    cluster_barrier();  // no CTA leaves while a peer may still read its shared memory
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        if (*abort_flag)
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        tmem_dealloc(tmem, kCols);
+    }
+}
+
 // ---------------------------------------------------------------- backward
 //
 // Gradients of the (O, P) forward for dout (of O) and dprobs (of P) given P
@@ -1924,6 +2221,134 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
         *why = "outer strides must be multiples of 8 elements (16 bytes)"; return false;
     }
     return true;
+}
+
+// ---- tensor-core decode / split-KV (host)
+namespace {
+// Cluster size, key chunk, ring stages and shared-memory layout of
+// tc_decode_kernel for C CTAs per cluster; false when it does not fit.
+bool plan_tc_decode(const Problem& p, int C, TcDecParams* dp, int* smem) {
+    const long long rows = p.group * p.Sq;
+    const long long chunk = (p.Skv + C - 1) / C;
+    const long long nt = (chunk + 127) / 128;
+    const int stages = nt <= 2 ? 2 : 3;
+    const long long shrink = stages == 2 ? DecLayout::kRingShrink2 : 0;
+    long long off = DecLayout::kFixed - shrink;
+    auto al = [](long long x) { return (x + 15) & ~15ll; };
+    const long long off_ss = off; off = al(off + rows * chunk * 4);
+    const long long off_part = off; off = al(off + rows * 128 * 4);
+    const long long off_st = off; off += rows * 2 * 4;
+    off += 1024;  // alignment slack of the dynamic base
+    if (off > kDecSmemMax) return false;
+    dp->chunk = (int)chunk;
+    dp->stages = stages;
+    dp->off_ss = (int)off_ss;
+    dp->off_part = (int)off_part;
+    dp->off_st = (int)off_st;
+    *smem = (int)off;
+    return true;
+}
+
+int tc_decode_cluster(const Problem& p) {
+    const long long c = (p.Skv + 255) / 256;
+    return (int)(c < 1 ? 1 : (c > kDecMaxCluster ? kDecMaxCluster : c));
+}
+
+std::mutex g_dec_mu;
+struct DecChoice { const void* kern; int dev; int smem; int C; };
+DecChoice g_dec[32];
+int g_ndec = 0;
+
+template <typename T>
+cudaError_t launch_tc_decode_t(const Problem& pr, cudaStream_t stream) {
+    TcDecParams p;
+    std::memset(&p, 0, sizeof(p));
+    CUtensorMap mk, mv;
+    if (!make_map(&mk, pr.dtype, pr.k, pr.D, pr.Skv, pr.Hkv, pr.B, pr.sk, 128, &p.ord_k) ||
+        !make_map(&mv, pr.dtype, pr.v, pr.Dv, pr.Skv, pr.Hkv, pr.B, pr.sv, 128, &p.ord_v))
+        return cudaErrorNotSupported;
+    p.q = pr.q; p.sq0 = pr.sq[0]; p.sq1 = pr.sq[1]; p.sq2 = pr.sq[2];
+    p.mask = pr.mask; p.mask_kind = pr.mask_kind; p.mask_dtype = pr.mask_dtype;
+    p.sm0 = pr.sm[0]; p.sm1 = pr.sm[1]; p.sm2 = pr.sm[2];
+    p.o = pr.o; p.so0 = pr.so[0]; p.so1 = pr.so[1]; p.so2 = pr.so[2];
+    p.p = pr.p; p.sp0 = pr.sp[0]; p.sp1 = pr.sp[1]; p.sp2 = pr.sp[2];
+    p.lse = pr.lse;
+    p.Hq = (int)pr.Hq; p.Sq = (int)pr.Sq; p.Skv = (int)pr.Skv; p.group = (int)pr.group;
+    p.rows = (int)(pr.group * pr.Sq); p.causal = pr.causal;
+    p.c2 = pr.scale * kLog2e;
+    auto kern = tc_decode_kernel<T>;
+    int C = tc_decode_cluster(pr), smem = 0;
+    if (!plan_tc_decode(pr, C, &p, &smem)) return cudaErrorNotSupported;
+    cudaError_t e = prepare_kernel(kern, kDecSmemMax, false);
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(kDecThreads, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (C > 8) {
+        // a cluster above the portable size needs the opt-in and a schedulable placement
+        std::lock_guard<std::mutex> lock(g_dec_mu);
+        int chosen = 0;
+        for (int i = 0; i < g_ndec; ++i)
+            if (g_dec[i].kern == reinterpret_cast<const void*>(kern) && g_dec[i].dev == dev && g_dec[i].smem == smem)
+                chosen = g_dec[i].C;
+        if (chosen == 0) {
+            int nc = 0;
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+                cfg.gridDim = dim3((unsigned)C, 1, 1);
+                cfg.dynamicSmemBytes = (size_t)smem;
+                attr[0].val.clusterDim.x = (unsigned)C;
+                if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) nc = 0;
+            }
+            (void)cudaGetLastError();
+            chosen = nc > 0 ? C : 8;
+            if (g_ndec < 32) g_dec[g_ndec++] = DecChoice{reinterpret_cast<const void*>(kern), dev, smem, chosen};
+        }
+        if (chosen != C) {
+            C = chosen;
+            if (!plan_tc_decode(pr, C, &p, &smem)) return cudaErrorNotSupported;
+        }
+    }
+    cfg.gridDim = dim3((unsigned)C, (unsigned)pr.Hkv, (unsigned)pr.B);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    e = cudaLaunchKernelEx(&cfg, kern, mk, mv, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+}  // namespace
+
+bool tc_decode_supports(const Problem& p, const char** why) {
+    if (p.dtype != kF16 && p.dtype != kBF16) { *why = "dtype must be f16 or bf16"; return false; }
+    if (p.D != 128 || p.Dv != 128) { *why = "head dims must be 128"; return false; }
+    if (p.group * p.Sq > 16) { *why = "more than 16 query rows per key/value head"; return false; }
+    if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
+    if (p.B > 65535 || p.Hkv > 65535 || p.Skv >= (1ll << 31)) { *why = "sizes beyond the grid limits"; return false; }
+    const int64_t eq[3] = {p.B, p.Hq, p.Sq}, ek[3] = {p.B, p.Hkv, p.Skv};
+    if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !strides_ok(p.sq, eq) || !strides_ok(p.sk, ek) ||
+        !strides_ok(p.sv, ek)) {
+        *why = "q, k and v rows must start on 16-byte boundaries"; return false;
+    }
+    TcDecParams dp;
+    int smem;
+    if (!plan_tc_decode(p, tc_decode_cluster(p), &dp, &smem)) {
+        *why = "the scores of a key chunk do not fit shared memory"; return false;
+    }
+    return true;
+}
+
+cudaError_t launch_tc_decode(const Problem& p, cudaStream_t stream) {
+    const char* why;
+    if (!tc_decode_supports(p, &why)) return cudaErrorNotSupported;
+    return p.dtype == kF16 ? launch_tc_decode_t<__half>(p, stream) : launch_tc_decode_t<__nv_bfloat16>(p, stream);
 }
 
 bool bwd_tc_supports(const BwdProblem& p, const char** why) {

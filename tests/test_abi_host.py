@@ -199,13 +199,14 @@ def test_f32_always_plans_simt(lib):
 
 # AUTO's kernel family per benchmark workload (host-only planning): the fused
 # single-sweep kernel for Skv <= 256, the cluster decode kernel for few rows
-# per KV head, the split-KV kernel when those rows meet a long key sequence,
+# per KV head, the tensor-core split-KV kernel when those rows meet a long key
+# sequence at D = 128 (the CUDA-core split-KV kernel at other head dims),
 # the one-tile two-pass kernel under a causal mask, the paired layout for the
 # non-causal GQA prefill, and the CUDA-core kernel for fp32.
 @pytest.mark.parametrize("name,expect", [
     ("tiny_f32", "simt"), ("prefill1k_d64_f16", "twopass"), ("prefill2k_d128_f16", "twopass"),
     ("prefill2k_d128_bf16", "twopass"), ("gqa1k_d128_f16", "paired"), ("decode_skv1152_f16", "decode"),
-    ("tail100_mask_f16", "fused"), ("decode_skv32k_f16", "split")])
+    ("tail100_mask_f16", "fused"), ("decode_skv32k_f16", "tcdecode")])
 def test_auto_choice_per_workload(lib, name, expect):
     from sdpa_forward_materialised_gb300 import workloads as W
     w = W.BY_NAME[name]
@@ -226,9 +227,11 @@ def test_fused_needs_at_most_256_keys(lib):
 
 
 def test_split_kv_limits(lib):
-    """Few rows and a long key sequence go to the split-KV kernel while the
-    scores of a 1/16 key chunk fit shared memory; past that, to the two-pass
-    tensor-core kernel (K and V are zero-stride views: planning reads no data)."""
+    """Few rows and a long key sequence go to a split-KV kernel while the
+    scores of a key chunk fit shared memory: the tensor-core one at D = Dv =
+    128 (f16 / bf16), the CUDA-core one at other head dims; past that, to the
+    two-pass tensor-core kernel.  K and V are zero-stride views: planning reads
+    no data."""
     def kv(Skv, D):
         base = torch.zeros(1, 1, 1, D, dtype=torch.float16)
         return base.expand(1, 1, Skv, D), base.expand(1, 1, Skv, D)
@@ -236,9 +239,16 @@ def test_split_kv_limits(lib):
     k, v = kv(2048, 128)
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "decode"
     k, v = kv(5000, 128)
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "tcdecode"
+    assert sm.sdpa_math_plan(q, k, v, variant="split")["variant"] == "split"
+    k, v = kv(65536, 128)                  # 4 rows x 4096 keys of scores: 64 KiB beside the 96 KiB K/V ring
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "tcdecode"
+    k, v = kv(131072, 128)                 # 128 KiB of scores: only the CUDA-core split kernel has room
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "split"
-    k, v = kv(131072, 128)                 # 4 rows x 8192 keys of scores: 128 KiB
-    assert sm.sdpa_math_plan(q, k, v)["variant"] == "split"
+    q64 = torch.zeros(1, 4, 1, 64, dtype=torch.float16)
+    k, v = kv(5000, 64)
+    assert sm.sdpa_math_plan(q64, k, v)["variant"] == "split"
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q64, k, v, variant="tcdecode"), "head dims must be 128")
     q16 = torch.zeros(1, 16, 1, 256, dtype=torch.float16)
     k, v = kv(4100, 256)
     assert sm.sdpa_math_plan(q16, k, v)["variant"] == "split"
@@ -247,9 +257,11 @@ def test_split_kv_limits(lib):
     q16 = torch.zeros(1, 16, 1, 128, dtype=torch.float16)
     k, v = kv(1 << 18, 128)                # 16 rows x 16384 keys of scores: 1 MiB
     assert sm.sdpa_math_plan(q16, k, v)["variant"] == "twopass"
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q16, k, v, variant="tcdecode"), "key chunk")
     q17 = torch.zeros(1, 17, 1, 128, dtype=torch.float16)
     k, v = kv(5000, 128)
     _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q17, k, v, variant="split"), "16 query rows")
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q17, k, v, variant="tcdecode"), "16 query rows")
 
 
 def _bwd_args(B=1, Hq=4, Hkv=2, Sq=9, Skv=11, D=16, Dv=8, dtype=torch.float16):

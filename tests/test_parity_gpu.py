@@ -68,7 +68,7 @@ def _full_check(q, k, v, mask, causal, scale, variant="auto", check_lse=True):
 def _variants_for(q, k, v, mask, causal):
     """Every kernel family that accepts this call (the SIMT one always does)."""
     out = []
-    for name in ("simt", "twopass", "paired", "fused", "decode", "split"):
+    for name in ("simt", "twopass", "paired", "fused", "decode", "split", "tcdecode"):
         try:
             sm.sdpa_math_plan(q, k, v, mask, is_causal=causal, variant=name)
             out.append(name)
@@ -146,6 +146,13 @@ SMALL = [
     (1, 16, 1, 1, 4100, 256, "f16", False, None),
     (1, 2, 1, 6, 2200, 64, "f16", True, None),
     (1, 4, 1, 1, 10, 64, "f16", False, None),
+    # the tensor-core decode kernel (D = 128): one-tile and multi-tile chunks,
+    # 16 rows, a bool mask with dead rows, causal rows, bf16, fewer keys than CTAs
+    (2, 8, 2, 1, 1152, 128, "f16", False, None),
+    (1, 16, 1, 1, 3000, 128, "bf16", False, None),
+    (2, 4, 2, 2, 777, 128, "f16", False, "bool"),
+    (1, 2, 1, 5, 600, 128, "f16", True, None),
+    (1, 4, 2, 1, 9, 128, "bf16", False, "additive"),
 ]
 
 
