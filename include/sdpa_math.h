@@ -153,15 +153,18 @@ typedef struct {
 
 /*
  * sdpa_math_plan -- validate exactly like sdpa_math_fwd and report the kernel
- * family the call would use.  The variant is chosen by the number of score
- * tiles that survive causal truncation, not by area (the page's fusion
- * criterion, "single-kernel fusion (small shapes)" update), with thresholds
- * set for GB300.  Between the two tensor-core two-pass layouts it picks
- * TC_PAIRED (two query tiles per CTA) for calls without a causal mask when the
- * paired grid still gives about one CTA per SM, else TC_TWOPASS.  `requested` is the variant the caller
- * would pass to sdpa_math_fwd_ex (AUTO = let the rule choose).  Data pointers
- * are checked for NULL and alignment but never dereferenced; the only CUDA
- * call is a query of the current device's SM count (nothing is enqueued).
+ * family the call would use.  AUTO's rule, in order: fp32 -> SIMT; at most 16
+ * query rows per KV head -> DECODE while a 1/8 key chunk fits it, else
+ * TC_DECODE (D = Dv = 128, f16/bf16), else SPLIT; otherwise the tensor-core
+ * families, chosen by the number of score tiles that survive causal truncation
+ * rather than by area (the page's fusion criterion, "single-kernel fusion
+ * (small shapes)" update): TC_FUSED up to 256 keys, then TC_PAIRED (two query
+ * tiles per CTA) for calls without a causal mask when the paired grid still
+ * gives about one CTA per SM, else TC_TWOPASS; SIMT when none accepts the
+ * layout.  `requested` is the variant the caller would pass to
+ * sdpa_math_fwd_ex (AUTO = let the rule choose).  Data pointers are checked
+ * for NULL and alignment but never dereferenced; the only CUDA call is a
+ * query of the current device's SM count (nothing is enqueued).
  */
 sdpa_status sdpa_math_plan(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
                            const sdpa_tensor *mask, sdpa_mask_kind mask_kind, int is_causal,

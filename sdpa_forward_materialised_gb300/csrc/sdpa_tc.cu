@@ -1114,8 +1114,7 @@ constexpr int kDecMaxCluster = 16;
 constexpr int kDecSmemMax = 220 * 1024;  // dynamic shared memory (the kernel also has a little static)
 struct DecLayout {
     static constexpr int kTile = 128 * 128 * 2;         // one K or V tile
-    static constexpr int kMaxStages = 3;
-    static constexpr int kOffRing = 0;
+    static constexpr int kMaxStages = 3;                // the ring starts at offset 0
     static constexpr int kOffQ = kMaxStages * kTile;     // [16 rows, 128] K-major
     static constexpr int kOffP = kOffQ + 4096;           // two [16 rows, 128 keys] P^T operands
     static constexpr int kOffBar = kOffP + 8192;
@@ -1406,8 +1405,7 @@ struct BwdIO {
     float scale;
 };
 
-constexpr int kBwdThreads = 256;
-static_assert(kBwdThreads == FusedCfg::kThreads, "load_tile_sw128 strides by the fused kernel's block size");
+constexpr int kBwdThreads = 256;  // two warpgroups: the same 128 TMEM lanes, two column halves
 
 
 // 16-byte chunk c (keys 8c .. 8c+7) of row r of a swizzled [128, 128] tile.
@@ -1428,36 +1426,6 @@ template <> __device__ __forceinline__ float2 unpack_pair<__nv_bfloat16>(uint32_
     return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w));
 }
 
-
-// Rows [0, nvalid) of a [rows, X] slice into a ROWS-row swizzled tile whose
-// 64-column halves sit ROWS * 128 bytes apart (rows past nvalid zero-filled).
-template <typename T, int ROWS>
-__device__ __forceinline__ void load_rows_sw128(uint32_t dst, const T* src, long long srow, int nvalid, int X) {
-    const int upr = X / 8;  // 16-byte units per row
-    for (int u = threadIdx.x; u < ROWS * upr; u += kBwdThreads) {
-        const int r = u / upr, c = u % upr;
-        const bool ok = r < nvalid;
-        const T* g = ok ? src + r * srow + c * 8 : src;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                         dst + (c >> 3) * (ROWS * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
-                     "l"(g), "r"(ok ? 16 : 0)
-                     : "memory");
-    }
-}
-
-// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice into a swizzled
-// [128, 64] tile (one 64-key half; partial chunks at the key edge zero-filled).
-template <typename T>
-__device__ __forceinline__ void load_ptile64_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
-    for (int u = threadIdx.x; u < 128 * 8; u += kBwdThreads) {
-        const int r = u >> 3, c = u & 7;
-        int bytes = (ncols - 8 * c) * 2;
-        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
-        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(sw_chunk(dst, r, c)), "l"(g), "r"(bytes)
-                     : "memory");
-    }
-}
 
 // Rows kernel layout: dO once, then a three-stage ring of 64-key steps
 // (V_j K-major, K_j MN-major, P_ij and dprobs_ij; E hi / lo overwrite the last two).
@@ -1683,22 +1651,6 @@ bwd_tc_rows_kernel(const __grid_constant__ CUtensorMap tm_go, const __grid_const
         if (*abort_flag)
             for (int i = 0; i < 200; ++i) __nanosleep(1000);
         tmem_dealloc(tmem, kCols);
-    }
-}
-
-// Rows [0, nrows) x keys [0, ncols) of a [rows, keys] slice into a swizzled
-// [64, 128] tile (two 64-key halves 8 KB apart; partial chunks zero-filled).
-template <typename T>
-__device__ __forceinline__ void load_ptile_q64_sw128(uint32_t dst, const T* src, long long srow, int nrows, int ncols) {
-    for (int u = threadIdx.x; u < 64 * 16; u += kBwdThreads) {
-        const int r = u >> 4, c = u & 15;
-        int bytes = (ncols - 8 * c) * 2;
-        bytes = r < nrows ? (bytes < 0 ? 0 : (bytes > 16 ? 16 : bytes)) : 0;
-        const T* g = bytes > 0 ? src + r * srow + c * 8 : src;
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                         dst + (c >> 3) * 8192 + r * 128 + (((c & 7) ^ (r & 7)) << 4)),
-                     "l"(g), "r"(bytes)
-                     : "memory");
     }
 }
 
