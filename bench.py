@@ -545,7 +545,9 @@ def run_ours_bwd(args, w: W.Workload):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "hbm_gbs": gbs, "algorithmic_bytes": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gbs / hbm_peak, "traffic": None,
+                     "frac": gbs / hbm_peak,
+                     # DRAM bytes of the rows + keys kernels per step, from the ncu summary
+                     "traffic": ncu_traffic(w, "bwd", key=f"{w.name}:bwd") if bwd_tc_eligible(w) else None,
                      "peak_source": f"{peak_src} (copy bandwidth, burst)"},
         "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * 2,
@@ -563,9 +565,10 @@ def run_ours_bwd(args, w: W.Workload):
     return 0
 
 
-def ncu_traffic(w: W.Workload, variant: str):
+def ncu_traffic(w: W.Workload, variant: str, key: str = None):
     """DRAM bytes per launch from the committed ncu summary, only when it was
-    taken on the kernel sources as they are now (else None)."""
+    taken on the kernel sources as they are now (else None).  ``key`` names a
+    summary other than the workload's forward one (e.g. its backward)."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
@@ -574,7 +577,7 @@ def ncu_traffic(w: W.Workload, variant: str):
         fp = _build.source_fingerprint()
         with open(path) as f:
             d = json.load(f)
-        ent = d.get(w.name)
+        ent = d.get(key or w.name)
         if ent and ent.get("sources") == fp and ent.get("variant") == variant:
             return ent["dram_bytes_per_launch"]
     except Exception:
