@@ -2182,8 +2182,9 @@ namespace {
 bool plan_tc_decode(const Problem& p, int C, TcDecParams* dp, int* smem) {
     const long long rows = p.group * p.Sq;
     const long long chunk = (p.Skv + C - 1) / C;
-    const long long nt = (chunk + 127) / 128;
-    const int stages = nt <= 2 ? 2 : 3;
+    // two stages keep a CTA near 110 KB (with 4 rows and 2048-key chunks), so
+    // two CTAs share an SM and cover each other's load latency
+    const int stages = 2;
     const long long shrink = stages == 2 ? DecLayout::kRingShrink2 : 0;
     long long off = DecLayout::kFixed - shrink;
     auto al = [](long long x) { return (x + 15) & ~15ll; };

@@ -241,10 +241,11 @@ def test_split_kv_limits(lib):
     k, v = kv(5000, 128)
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "tcdecode"
     assert sm.sdpa_math_plan(q, k, v, variant="split")["variant"] == "split"
-    k, v = kv(65536, 128)                  # 4 rows x 4096 keys of scores: 64 KiB beside the 96 KiB K/V ring
+    k, v = kv(131072, 128)                 # 4 rows x 8192 keys of scores: 128 KiB beside the 64 KiB K/V ring
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "tcdecode"
-    k, v = kv(131072, 128)                 # 128 KiB of scores: only the CUDA-core split kernel has room
-    assert sm.sdpa_math_plan(q, k, v)["variant"] == "split"
+    assert sm.sdpa_math_plan(q, k, v, variant="split")["variant"] == "split"
+    k, v = kv(1 << 18, 128)                # 256 KiB of scores: neither split kernel has room
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "twopass"
     q64 = torch.zeros(1, 4, 1, 64, dtype=torch.float16)
     k, v = kv(5000, 64)
     assert sm.sdpa_math_plan(q64, k, v)["variant"] == "split"
