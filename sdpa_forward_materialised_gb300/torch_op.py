@@ -129,12 +129,15 @@ _override_lib: Optional[torch.library.Library] = None
 
 def enable_aten_override() -> None:
     """Run ``aten::_scaled_dot_product_attention_math`` on CUDA tensors through
-    the custom op (forward and backward).  Idempotent."""
+    the custom op (forward and backward).  Registered for AutogradCUDA (calls
+    under autograd) and for CUDA (calls that skip the autograd keys, e.g. under
+    ``torch.inference_mode()``).  Idempotent."""
     global _override_lib
     if _override_lib is not None:
         return
     lib = torch.library.Library("aten", "IMPL")
     lib.impl("_scaled_dot_product_attention_math", _aten_math_override, "AutogradCUDA")
+    lib.impl("_scaled_dot_product_attention_math", _aten_math_override, "CUDA")
     _override_lib = lib
 
 

@@ -56,15 +56,16 @@ def test_override_refuses_dropout_and_bad_heads():
 
 def test_override_enable_disable_dispatch_entry():
     assert not T.aten_override_enabled()
-    has = lambda: torch._C._dispatch_has_kernel_for_dispatch_key(KEY, "AutogradCUDA")
-    assert not has()
+    has = lambda key: torch._C._dispatch_has_kernel_for_dispatch_key(KEY, key)
+    assert not has("AutogradCUDA") and not has("CUDA")
     T.enable_aten_override()
     try:
         T.enable_aten_override()  # idempotent
-        assert T.aten_override_enabled() and has()
+        # under autograd, and for calls that skip the autograd keys (inference mode)
+        assert T.aten_override_enabled() and has("AutogradCUDA") and has("CUDA")
     finally:
         T.disable_aten_override()
-    assert not T.aten_override_enabled() and not has()
+    assert not T.aten_override_enabled() and not has("AutogradCUDA") and not has("CUDA")
     # CPU tensors never reach the override: the stock math path still runs there
     q = torch.randn(1, 2, 3, 4)
     o, p = torch.ops.aten._scaled_dot_product_attention_math(q, q, q)

@@ -66,6 +66,9 @@ def test_aten_override_under_the_math_backend():
     try:
         O_at, P_at = torch.ops.aten._scaled_dot_product_attention_math(qd, kd, vd, is_causal=True, enable_gqa=True)
         assert torch.equal(O_at, O_op) and torch.equal(P_at, P_op)
+        with torch.inference_mode():  # the autograd keys are skipped: the CUDA-key entry serves the call
+            O_im, P_im = torch.ops.aten._scaled_dot_product_attention_math(qd, kd, vd, is_causal=True, enable_gqa=True)
+        assert torch.equal(O_im, O_op) and torch.equal(P_im, P_op)
         qg, kg, vg = (t.clone().requires_grad_(True) for t in (qd, kd, vd))
         with sdpa_kernel(SDPBackend.MATH):
             out = torch.nn.functional.scaled_dot_product_attention(qg, kg, vg, is_causal=True, enable_gqa=True)
