@@ -5,9 +5,12 @@ One step = one materialised-probability SDPA forward over the workload: scores,
 masking, row statistics, exact P = exp(S - lse), P V and the stores of O and P,
 all in the library's CUDA kernels, called through the C ABI.
 
-Default workload: prefill 1k D64 (fp16, B=2, H=8, Sq=Skv=1024, D=64, causal),
-the shape of the perf-gate baseline of FlagOS-OP PR #10 "feat: add sdpa_math
-operator".  ``--config`` selects another of the synthetic workloads.
+Default workload: prefill 2k D128 (fp16, B=1, H=16, Sq=Skv=2048, D=128,
+causal), the shape FlagOS-OP PR #10 "feat: add sdpa_math operator" quotes its
+headline numbers on (first report's table: Ascend 910 Triton 1.369 ms against
+2.776 ms for the native math backend; the P800 table: 2.392 ms), and the
+largest single-GPU workload.  ``--config`` selects another of the synthetic
+workloads.
 
 Timing: W warm-up steps, then exactly K timed steps, each bracketed by CUDA
 events on the launching stream.  Before every step L2 is flushed by writing a
@@ -93,36 +96,113 @@ def load_peaks():
 
 # ----------------------------------------------------------------------------- clocks
 
+class NvmlClocks:
+    """In-process NVML queries (read-only: clocks, power, clock-event reasons)
+    through ctypes, so the timed region gets samples however short it is."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:  # the physical GPU behind the torch device, by UUID
+            uuid = str(torch.cuda.get_device_properties(torch_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = int(vis.split(",")[torch_index]) if vis and vis.split(",")[0].isdigit() else torch_index
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle")
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm))        # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reason_fn(self.h, ct.byref(rs))
+        return float(sm.value), float(mx.value), mw.value / 1000.0, int(rs.value)
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples while the timed region runs."""
+    """SM clock and clock-event reasons sampled every ~1 ms by a host thread
+    through NVML while the timed region runs (falls back to nvidia-smi at
+    100 ms when NVML cannot be loaded)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.samples = []
+    def __init__(self, torch_index: int, smi_index: int):
+        self.torch_index = torch_index
+        self.gpu = smi_index
+        self.samples = []  # (time, sm_mhz, max_mhz, watts, [reasons])
         self.proc = None
         self.thread = None
+        self.stop_flag = threading.Event()
+        self.source = None
 
     def start(self):
+        try:
+            nv = NvmlClocks(self.torch_index)
+            self.source = "nvml (in-process, ~1 ms)"
+            self.thread = threading.Thread(target=self._poll_nvml, args=(nv,), daemon=True)
+            self.thread.start()
+            return
+        except Exception:
+            pass
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-i", str(self.gpu), "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi (100 ms)"
         except (OSError, FileNotFoundError):
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _poll_nvml(self, nv):
+        while not self.stop_flag.is_set():
+            try:
+                sm, mx, w, rs = nv.sample()
+            except Exception:
+                return
+            self.samples.append((time.perf_counter(), sm, mx, w,
+                                 [n for bit, n in NvmlClocks.REASONS.items() if rs & bit]))
+            time.sleep(0.001)
+
+    def _read_smi(self):
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.proc.stdout:
-            self.samples.append((time.perf_counter(), line.strip()))
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm, mx = float(p[1]), float(p[2])
+            except ValueError:
+                continue
+            try:
+                w = float(p[3])
+            except ValueError:
+                w = None
+            self.samples.append((time.perf_counter(), sm, mx, w,
+                                 [n for n, val in zip(names, p[5:9]) if val.lower().startswith("active")]))
 
     def stop(self):
+        self.stop_flag.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -133,34 +213,27 @@ class ClockSampler:
             self.thread.join(timeout=5)
 
     def summary(self, t0: float, t1: float):
-        rows = []
-        for ts, line in self.samples:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            rows.append((ts, parts))
+        rows = list(self.samples)
         inside = [r for r in rows if t0 <= r[0] <= t1]
         use = inside if inside else sorted(rows, key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))[:1]
         if not use:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_region": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        sm_mhz, max_mhz = [], []
-        for _, p in use:
-            try:
-                sm_mhz.append(float(p[1]))
-                max_mhz.append(float(p[2]))
-            except ValueError:
-                pass
-            for n, val in zip(names, p[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm_mhz) if sm_mhz else None,
-                "sm_max_mhz": max(max_mhz) if max_mhz else None,
-                "reasons": sorted(reasons), "samples_in_region": len(inside)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples_in_region": 0,
+                    "source": self.source}
+        reasons = sorted({n for r in use for n in r[4]})
+        watts = [r[3] for r in use if r[3] is not None]
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "sm_mhz_min": min(r[1] for r in use), "power_w_max": max(watts) if watts else None,
+                "reasons": reasons, "samples_in_region": len(inside), "source": self.source}
 
 
 # ----------------------------------------------------------------------------- distributed
+
+def smi_index(local: int) -> int:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis and vis.split(",")[0].strip().isdigit():
+        return int(vis.split(",")[local])
+    return local
+
 
 def dist_setup(backend: str):
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -318,8 +391,7 @@ def run_ours(args, w: W.Workload):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = ClockSampler(local, smi_index(local))
     sampler.start()
     time.sleep(0.3)
     barrier(world)
@@ -392,6 +464,9 @@ def run_ours(args, w: W.Workload):
         "hbm_gbs": gbs, "algorithmic_bytes": nbytes,
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gbs / hbm_peak, "traffic": traffic,
+                     "traffic_kind": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch; DRAM only: "
+                                      "ncu flushes the caches before its replay, and P lines still dirty in the "
+                                      "129 MB L2 when the kernel ends are written back after it, uncounted"),
                      "peak_source": f"{peak_src} (copy bandwidth, burst)"},
         "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * plan["launches"],
@@ -482,8 +557,7 @@ def run_ours_bwd(args, w: W.Workload):
     sm.sdpa_math_device_status(stream)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler = ClockSampler(local, smi_index(local))
     sampler.start()
     time.sleep(0.3)
     barrier(world)
@@ -591,7 +665,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="prefill1k_d64_f16", choices=sorted(W.BY_NAME))
+    ap.add_argument("--config", default="prefill2k_d128_f16", choices=sorted(W.BY_NAME))
     ap.add_argument("--variant", default="auto",
                     choices=["auto", "simt", "twopass", "paired", "fused", "decode", "split", "tcdecode"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")

@@ -28,7 +28,12 @@
  *     four strides counted in ELEMENTS.  The innermost stride must be 1 (the
  *     page's "_d1(): only stride(-1) == 1 is required", micro-optimisation
  *     item of the 2026-10-02 update); the other strides are free, so
- *     transposed [B,S,H,D] storage is accepted without a copy.
+ *     transposed [B,S,H,D] storage is accepted without a copy.  Inputs may
+ *     be broadcast views (stride 0 over a batch, head or row dimension, as
+ *     torch's expand() makes); the tensor-core families that read 128-row
+ *     TMA tiles serve batch and head broadcasts and leave broadcast rows to
+ *     the other families.  Outputs must not overlap themselves: a stride-0
+ *     dimension of extent > 1 in out, probs, dq, dk or dv is an error.
  *   - The caller owns every buffer and the stream.  The library allocates no
  *     device memory per call and keeps no pointer after the call returns.
  *   - out and probs are written in full (every element, including the zeros
@@ -116,8 +121,9 @@ typedef struct {
  * q/k/v/out/probs, B mismatch, K and V disagreeing on Skv or Hkv, q and k
  * disagreeing on D, Hq % Hkv != 0, causal together with a mask, a mask shape
  * outside {1,B} x {1,Hq} x Sq x Skv, a mask dtype not allowed for its kind,
- * an innermost stride != 1, out or probs with the wrong shape, a data pointer
- * not aligned to its element size, or a non-finite scale.  Returns
+ * an innermost stride != 1, out or probs with the wrong shape or with a
+ * stride-0 dimension of extent > 1, a data pointer not aligned to its
+ * element size, or a non-finite scale.  Returns
  * SDPA_ERR_UNSUPPORTED for D or Dv > 256 or an input dtype that is not
  * f32/f16/bf16.
  */

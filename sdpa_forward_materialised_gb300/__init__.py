@@ -295,6 +295,30 @@ def empty_outputs(q, v, Skv, dtype=None):
     return O, P
 
 
+def prepare_mask(attn_mask, B: int, Hq: int, Sq: int, Skv: int, dtype):
+    """A mask broadcastable to [B, Hq, Sq, Skv] (bool, or additive of any
+    floating type) as the C ABI takes it: [1|B, 1|Hq, Sq, Skv] with unit
+    innermost stride.  Broadcast query / key dimensions (a key-padding mask
+    [B, 1, 1, Skv], say) are materialised; batch and head dimensions of extent
+    1 stay broadcast; an additive mask of another floating type becomes fp32."""
+    import torch
+    if attn_mask is None:
+        return None
+    m = attn_mask
+    if m.dtype != torch.bool and m.dtype not in (dtype, torch.float32):
+        m = m.to(torch.float32)
+    while m.dim() < 4:
+        m = m.unsqueeze(0)
+    if m.dim() != 4:
+        raise ValueError(f"attn_mask must have at most 4 dimensions, got {attn_mask.dim()}")
+    mb = B if m.shape[0] != 1 else 1
+    mh = Hq if m.shape[1] != 1 else 1
+    m = m.expand(mb, mh, Sq, Skv)
+    if m.stride(2) == 0 or m.stride(3) != 1:
+        m = m.contiguous()
+    return m
+
+
 def sdpa_math(q, k, v, attn_mask=None, dropout_p: float = 0.0, is_causal: bool = False,
               scale: Optional[float] = None, variant: str = "auto", return_lse: bool = False,
               stream=None):
@@ -311,10 +335,7 @@ def sdpa_math(q, k, v, attn_mask=None, dropout_p: float = 0.0, is_causal: bool =
         raise ValueError("dropout_p must be 0: dropout is not part of this operation")
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1]) if q.shape[-1] > 0 else 1.0
-    mask = attn_mask
-    if mask is not None:
-        while mask.dim() < 4:
-            mask = mask.unsqueeze(0)
+    mask = prepare_mask(attn_mask, q.shape[0], q.shape[1], q.shape[2], k.shape[-2], q.dtype)
     O, P = empty_outputs(q, v, k.shape[-2])
     lse = None
     if return_lse:

@@ -97,6 +97,18 @@ sdpa_status check_tensor(const sdpa_tensor* t, const char* name) {
     return SDPA_OK;
 }
 
+// An output must not overlap itself: no dimension of extent > 1 may have
+// stride 0 (a broadcast view), or its elements would be written by several
+// threads at once.
+sdpa_status check_output(const sdpa_tensor* t, const char* name) {
+    for (int i = 0; i < 4; ++i)
+        if (t->shape[i] > 1 && t->stride[i] == 0)
+            return fail(SDPA_ERR_INVALID_ARGUMENT,
+                        "%s: dimension %d has stride 0 over %lld elements (an output must not overlap itself)",
+                        name, i, (long long)t->shape[i]);
+    return SDPA_OK;
+}
+
 bool same_shape(const sdpa_tensor* t, int64_t a, int64_t b, int64_t c, int64_t d) {
     return t->shape[0] == a && t->shape[1] == b && t->shape[2] == c && t->shape[3] == d;
 }
@@ -111,6 +123,8 @@ sdpa_status validate(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tens
     if ((s = check_tensor(v, "v")) != SDPA_OK) return s;
     if ((s = check_tensor(out, "out")) != SDPA_OK) return s;
     if ((s = check_tensor(probs, "probs")) != SDPA_OK) return s;
+    if ((s = check_output(out, "out")) != SDPA_OK) return s;
+    if ((s = check_output(probs, "probs")) != SDPA_OK) return s;
 
     if (q->dtype != SDPA_F32 && q->dtype != SDPA_F16 && q->dtype != SDPA_BF16)
         return fail(SDPA_ERR_UNSUPPORTED, "q: dtype %s is not f32/f16/bf16", dtype_name(q->dtype));
@@ -295,14 +309,22 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
         case SDPA_VARIANT_TC_DECODE: e = sdpa::launch_tc_decode(p, st); break;
         default: e = sdpa::launch_simt(p, st); break;
     }
-    // A tensor-core family refuses (before launching anything) when the
-    // driver will not encode a TMA descriptor for this layout; AUTO then
-    // serves the call with the CUDA-core kernel, a forced family reports it.
+    // A family can still refuse at launch, before enqueuing anything: the
+    // driver will not encode a TMA descriptor for this layout, or (TC_DECODE)
+    // only the portable 8-CTA cluster can be scheduled and a key chunk of that
+    // cluster does not fit shared memory.  AUTO then serves the call with the
+    // split-KV kernel where it can, else the CUDA-core kernel; a forced family
+    // reports it.
     if (e == cudaErrorNotSupported && chosen != SDPA_VARIANT_SIMT) {
         (void)cudaGetLastError();
         if (variant != SDPA_VARIANT_AUTO || env_variant() != SDPA_VARIANT_AUTO)
-            return fail(SDPA_ERR_UNSUPPORTED, "the forced kernel family cannot encode TMA descriptors for this layout");
-        e = sdpa::launch_simt(p, st);
+            return fail(SDPA_ERR_UNSUPPORTED,
+                        "the forced kernel family refused its launch: the driver would not encode a TMA "
+                        "descriptor for this layout, or the cluster size that can be scheduled leaves a key "
+                        "chunk too large for shared memory");
+        const char* why = nullptr;
+        if (chosen == SDPA_VARIANT_TC_DECODE && sdpa::split_supports(p, &why)) e = sdpa::launch_split(p, st);
+        else e = sdpa::launch_simt(p, st);
     }
     if (e != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -344,6 +366,8 @@ sdpa_status sdpa_math_bwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
     const char* names[] = {"q", "k", "v", "probs", "dout", "dq", "dk", "dv"};
     for (int i = 0; i < 8; ++i)
         if ((s = check_tensor(all[i], names[i])) != SDPA_OK) return s;
+    for (int i = 5; i < 8; ++i)
+        if ((s = check_output(all[i], names[i])) != SDPA_OK) return s;
     if (dprobs && (s = check_tensor(dprobs, "dprobs")) != SDPA_OK) return s;
     if (q->dtype != SDPA_F32 && q->dtype != SDPA_F16 && q->dtype != SDPA_BF16)
         return fail(SDPA_ERR_UNSUPPORTED, "q: dtype %s is not f32/f16/bf16", dtype_name(q->dtype));

@@ -816,6 +816,7 @@ bool decode_supports(const Problem& p, const char** why) {
     if (p.group * p.Sq > kMaxRows) { *why = "more than 16 query rows per key/value head"; return false; }
     if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
     if (p.D > 256 || p.Dv > 256) { *why = "head dim above 256"; return false; }
+    if (p.D < 1 || p.Dv < 1) { *why = "empty head dim"; return false; }
     if (p.B > 65535 || p.Hkv > 65535 || p.Skv >= (1ll << 31)) { *why = "sizes beyond the grid limits"; return false; }
     const int es = elem_bytes(p.dtype);
     if ((p.D * es) % 16 != 0 || (p.Dv * es) % 16 != 0) { *why = "head dims must be 16-byte multiples"; return false; }
@@ -836,6 +837,7 @@ bool split_supports(const Problem& p, const char** why) {
     if (p.group * p.Sq > kMaxRows) { *why = "more than 16 query rows per key/value head"; return false; }
     if (p.Sq < 1 || p.Skv < 1) { *why = "empty sequence"; return false; }
     if (p.D > 256 || p.Dv > 256) { *why = "head dim above 256"; return false; }
+    if (p.D < 1 || p.Dv < 1) { *why = "empty head dim"; return false; }
     if (p.B > 65535 || p.Hkv > 65535 || p.Skv >= (1ll << 31)) { *why = "sizes beyond the grid limits"; return false; }
     const int es = elem_bytes(p.dtype);
     if ((p.D * es) % 16 != 0 || (p.Dv * es) % 16 != 0) { *why = "head dims must be 16-byte multiples"; return false; }

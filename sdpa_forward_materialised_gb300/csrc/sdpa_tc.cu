@@ -69,8 +69,10 @@ constexpr uint32_t kRegsLow = 72, kRegsHigh = 208;
 // The three outer tensor-map dimensions are stored in stride order; a packed
 // code (2 bits per slot) says which logical dimension (1 = rows, 2 = head,
 // 3 = batch) sits at tensor-map dim k+1, and pick() maps coordinates to it.
+// Code 0 marks a broadcast dimension (stride 0 in the caller's view): the map
+// holds it with extent 1 and every coordinate along it is 0.
 __device__ __forceinline__ int pick(uint32_t sel, int rows, int head, int batch) {
-    return sel == 1 ? rows : (sel == 2 ? head : batch);
+    return sel == 1 ? rows : (sel == 2 ? head : (sel == 3 ? batch : 0));
 }
 
 struct TcParams {
@@ -1914,6 +1916,10 @@ bool encode_map(CUtensorMap* map, int dtype, const void* base, long long X, long
     if (!fn) return false;
     struct Dim { long long ext, stride; int sel; };
     Dim d[3] = {{S, st[2], 1}, {H, st[1], 2}, {Bn, st[0], 3}};
+    // a broadcast dimension (stride 0, every index reads the same memory)
+    // becomes an extent-1 dimension whose coordinate is always 0 (code 0)
+    for (auto& x : d)
+        if (x.ext > 1 && x.stride == 0) { x.ext = 1; x.sel = 0; }
     // extent-1 dims never move: give them a stride past everything else
     long long maxb = X;
     for (auto& x : d) if (x.ext > 1) maxb = std::max(maxb, x.stride * x.ext);
@@ -1988,6 +1994,11 @@ bool strides_ok(const int64_t* st, const int64_t* ext) {
         if (ext[i] > 1 && st[i] % 8 != 0) return false;
     return true;
 }
+
+// A tensor whose rows are broadcast (row stride 0 over more than one row)
+// cannot be read as 128-row TMA boxes; batch and head broadcasts can (see
+// encode_map).
+bool rows_broadcast(const int64_t* st, int64_t rows) { return rows > 1 && st[2] == 0; }
 
 // One-time (per kernel instantiation and device) launch preparation: the
 // register check of the in-kernel split and the shared-memory opt-in.  Keyed
@@ -2172,6 +2183,9 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
         !strides_ok(p.so, eq)) {
         *why = "outer strides must be multiples of 8 elements (16 bytes)"; return false;
     }
+    if (rows_broadcast(p.sq, p.Sq) || rows_broadcast(p.sk, p.Skv) || rows_broadcast(p.sv, p.Skv)) {
+        *why = "q, k or v rows are broadcast (row stride 0): TMA tiles need distinct rows"; return false;
+    }
     return true;
 }
 
@@ -2290,6 +2304,9 @@ bool tc_decode_supports(const Problem& p, const char** why) {
         !strides_ok(p.sv, ek)) {
         *why = "q, k and v rows must start on 16-byte boundaries"; return false;
     }
+    if (rows_broadcast(p.sk, p.Skv) || rows_broadcast(p.sv, p.Skv)) {
+        *why = "k or v rows are broadcast (row stride 0): TMA tiles need distinct rows"; return false;
+    }
     TcDecParams dp;
     int smem;
     if (!plan_tc_decode(p, tc_decode_cluster(p), &dp, &smem)) {
@@ -2323,6 +2340,10 @@ bool bwd_tc_supports(const BwdProblem& p, const char** why) {
     // P and dprobs rows are read in 16-byte chunks from their own start
     if ((p.Sq > 1 && p.sp[2] % 8 != 0) || (p.dprobs && p.Sq > 1 && p.sgp[2] % 8 != 0)) {
         *why = "probs and dprobs rows must start on 16-byte boundaries"; return false;
+    }
+    if (rows_broadcast(p.sq, p.Sq) || rows_broadcast(p.sp, p.Sq) || rows_broadcast(p.sgo, p.Sq) ||
+        (p.dprobs && rows_broadcast(p.sgp, p.Sq)) || rows_broadcast(p.sk, p.Skv) || rows_broadcast(p.sv, p.Skv)) {
+        *why = "an input's rows are broadcast (row stride 0): TMA tiles need distinct rows"; return false;
     }
     return true;
 }

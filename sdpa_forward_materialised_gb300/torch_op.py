@@ -28,7 +28,7 @@ from typing import Optional, Tuple
 import torch
 from torch import Tensor
 
-from . import sdpa_math_backward, sdpa_math_fwd_ex, _mask_kind
+from . import prepare_mask, sdpa_math_backward, sdpa_math_fwd_ex, _mask_kind
 
 _NS = "sdpa_gb300"
 
@@ -39,24 +39,8 @@ def _inner_contig(t: Tensor) -> Tensor:
 
 def _prepare_mask(attn_mask: Optional[Tensor], B: int, Hq: int, Sq: int, Skv: int,
                   dtype: torch.dtype) -> Optional[Tensor]:
-    """Broadcast a mask to [1|B, 1|Hq, Sq, Skv] (the shape the library takes);
-    query and key dimensions that were broadcast are materialised, and an
-    additive mask of another floating type is converted to fp32."""
-    if attn_mask is None:
-        return None
-    m = attn_mask
-    if m.dtype != torch.bool and m.dtype not in (dtype, torch.float32):
-        m = m.to(torch.float32)
-    while m.dim() < 4:
-        m = m.unsqueeze(0)
-    if m.dim() != 4:
-        raise ValueError(f"attn_mask must have at most 4 dimensions, got {attn_mask.dim()}")
-    mb = B if m.shape[0] != 1 else 1
-    mh = Hq if m.shape[1] != 1 else 1
-    m = m.expand(mb, mh, Sq, Skv)
-    if m.stride(2) == 0 or m.stride(3) != 1:
-        m = m.contiguous()
-    return m
+    """Broadcast a mask to [1|B, 1|Hq, Sq, Skv] (the shape the library takes)."""
+    return prepare_mask(attn_mask, B, Hq, Sq, Skv, dtype)
 
 
 def _default_scale(q: Tensor, scale: Optional[float]) -> float:
@@ -75,8 +59,10 @@ def sdpa_math_op(q: Tensor, k: Tensor, v: Tensor, attn_mask: Optional[Tensor], i
     mask = _prepare_mask(attn_mask, B, Hq, Sq, Skv, q.dtype)
     O = q.new_empty((B, Hq, Sq, v.shape[-1]))
     P = q.new_empty((B, Hq, Sq, Skv))
-    sdpa_math_fwd_ex(q, k, v, mask, _mask_kind(mask), is_causal, _default_scale(q, scale), O, P, None,
-                     "auto", torch.cuda.current_stream(q.device))
+    # the library launches on the current device: make it the tensors' device
+    with torch.cuda.device(q.device):
+        sdpa_math_fwd_ex(q, k, v, mask, _mask_kind(mask), is_causal, _default_scale(q, scale), O, P, None,
+                         "auto", torch.cuda.current_stream(q.device))
     return O, P
 
 
@@ -101,8 +87,9 @@ def _backward(ctx, dO, dP):
     dO = _inner_contig(dO.to(q.dtype))
     if dP is not None:
         dP = _inner_contig(dP.to(q.dtype))
-    dq, dk, dv = sdpa_math_backward(q, k, v, P, dO, dP, scale=ctx.scale,
-                                    stream=torch.cuda.current_stream(q.device))
+    with torch.cuda.device(q.device):
+        dq, dk, dv = sdpa_math_backward(q, k, v, P, dO, dP, scale=ctx.scale,
+                                        stream=torch.cuda.current_stream(q.device))
     return dq, dk, dv, None, None, None
 
 

@@ -1,14 +1,18 @@
 """Comparison helpers for the GPU-vs-oracle parity tests.
 
-Tolerances (max-abs, on both O and P): f32 1e-5, f16 2e-3, bf16 8e-3.  Where
-the output dtype cannot represent the exact value that closely (bf16 values of
-magnitude >= 4 have a half-ulp of 1.6e-2), an element may instead be off by at
-most one ulp of the dtype at the reference's magnitude.  For O that allowance
-also carries the rounding of P: the operation returns P in the input dtype and
-O = P V is formed from that rounded P (as the math backend does), so O may
-additionally differ from the exact fp64 value by sum_j half-ulp(P_ij) * |V_j|.
-The number of elements that needed an allowance beyond the plain tolerance
-is reported.
+Tolerances (max-abs, on both O and P): f32 1e-5, f16 2e-3, bf16 8e-3.
+
+f32 and f16 are held to the plain max-abs bound on every element: both
+dtypes can represent the results that closely (the f16 half-ulp is 1.95e-3
+for magnitudes in [4, 8)).
+
+bf16 cannot: its half-ulp at magnitudes in [4, 8) is 1.6e-2, twice the
+bound, so a correctly rounded bf16 O can miss 8e-3.  For bf16 only, an
+element may instead be off by one bf16 ulp at the reference's magnitude, and
+for O also by sum_j half-ulp(P_ij) * |V_j|: the operation returns P in the
+input dtype and O = P V is formed from that rounded P (as the math backend
+does).  compare() counts the bf16 elements that needed this allowance and
+prints the count with the plain max-abs error.
 """
 import numpy as np
 import torch
@@ -50,8 +54,10 @@ def o_allowance(p_ref: np.ndarray, v, group: int, dtype, rows=None, Hq=None, Sq=
 def compare(got, ref, dtype, what="", extra=None):
     """Element-wise check; returns a stats dict, raises AssertionError on failure.
 
-    The allowance per element is max(tol, ulp(|ref|) + extra): ``extra`` is
-    the propagated rounding of P for O (``o_allowance``), None for P."""
+    f32 / f16: every element within the plain max-abs tolerance.  bf16: the
+    allowance per element is max(tol, ulp(|ref|) + extra), ``extra`` being the
+    propagated rounding of P for O (``o_allowance``), None for P; the count of
+    elements beyond the plain tolerance is printed."""
     g = got.detach().double().cpu().numpy() if torch.is_tensor(got) else np.asarray(got, np.float64)
     r = np.asarray(ref, dtype=np.float64)
     assert g.shape == r.shape, f"{what}: shape {g.shape} vs {r.shape}"
@@ -60,14 +66,21 @@ def compare(got, ref, dtype, what="", extra=None):
     assert not np.isnan(g).any(), f"{what}: NaN in GPU output (unwritten or bad)"
     err = np.abs(g - r)
     tol = TOL[dtype]
-    allow = np.maximum(tol, ulp(r, dtype) + (0.0 if extra is None else extra))
+    if dtype == torch.bfloat16:
+        allow = np.maximum(tol, ulp(r, dtype) + (0.0 if extra is None else extra))
+    else:
+        allow = np.full(err.shape, tol)
     bad = err > allow
     if bad.any():
         idx = np.unravel_index(np.argmax(err - allow), err.shape)
         raise AssertionError(
             f"{what}: {int(bad.sum())} elements beyond tolerance; worst at {idx}: "
             f"got {g[idx]!r} ref {r[idx]!r} err {err[idx]:.3e} allow {allow[idx]:.3e}")
-    return {"max_abs": float(err.max()), "ulp_allowance_used": int((err > tol).sum())}
+    used = int((err > tol).sum())
+    if dtype == torch.bfloat16:
+        print(f"[parity] {what}: max-abs {float(err.max()):.3e}, bf16 elements beyond {tol:g} "
+              f"inside the ulp allowance: {used}")
+    return {"max_abs": float(err.max()), "ulp_allowance_used": used}
 
 
 def row_sum_bound(dtype, skv: int) -> float:

@@ -230,11 +230,12 @@ def test_split_kv_limits(lib):
     """Few rows and a long key sequence go to a split-KV kernel while the
     scores of a key chunk fit shared memory: the tensor-core one at D = Dv =
     128 (f16 / bf16), the CUDA-core one at other head dims; past that, to the
-    two-pass tensor-core kernel.  K and V are zero-stride views: planning reads
-    no data."""
+    two-pass tensor-core kernel.  K and V are views whose rows overlap (row
+    stride 16 bytes): planning reads no data."""
     def kv(Skv, D):
-        base = torch.zeros(1, 1, 1, D, dtype=torch.float16)
-        return base.expand(1, 1, Skv, D), base.expand(1, 1, Skv, D)
+        base = torch.zeros((Skv - 1) * 8 + D, dtype=torch.float16)
+        t = base.as_strided((1, 1, Skv, D), (0, 0, 8, 1))
+        return t, t
     q = torch.zeros(1, 4, 1, 128, dtype=torch.float16)
     k, v = kv(2048, 128)
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "decode"
@@ -316,3 +317,44 @@ def test_backward_argument_errors(lib):
     q6, k6, v6, P6, go6, dq6, dk6, dv6 = _bwd_args(Hq=6, Hkv=4)
     _expect("SDPA_ERR_INVALID_ARGUMENT",
             lambda: sm.sdpa_math_bwd(q6, k6, v6, P6, go6, None, 0.25, dq6, dk6, dv6, rs, stream=0), "divisible")
+
+
+def test_empty_value_head_dim_with_aligned_rows_plans_without_crashing(lib):
+    """A V with Dv = 0 but a 16-byte row stride (a slice v[..., :0] of a
+    contiguous tensor) over a long key sequence: the split-KV planners must
+    refuse it (they size work per pair of value columns) rather than divide
+    by zero on the host."""
+    q = torch.zeros(1, 8, 1, 128, dtype=torch.float16)
+    k = torch.zeros(1, 8, 4096, 128, dtype=torch.float16)
+    vbase = torch.zeros(1, 8, 4096, 8, dtype=torch.float16)
+    v = vbase[..., :0]
+    assert v.stride(2) == 8
+    r = sm.sdpa_math_plan(q, k, v)
+    assert r["variant"] == "simt"
+    for forced in ("decode", "split", "tcdecode"):
+        _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant=forced))
+
+
+def test_outputs_must_not_overlap_themselves(lib):
+    """An out or probs view with stride 0 over more than one element would be
+    written by several threads at once: refused on the host."""
+    q, k, v = _qkv()
+    O = torch.zeros(2, 4, 1, 64, dtype=torch.float16).expand(2, 4, 33, 64)
+    P = torch.zeros(2, 4, 33, 47, dtype=torch.float16)
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_plan(q, k, v, out=O, probs=P), "must not overlap")
+    O = torch.zeros(2, 4, 33, 64, dtype=torch.float16)
+    P = torch.zeros(1, 4, 33, 47, dtype=torch.float16).expand(2, 4, 33, 47)
+    _expect("SDPA_ERR_INVALID_ARGUMENT",
+            lambda: sm.sdpa_math_plan(q, k, v, out=O, probs=P), "must not overlap")
+
+
+def test_broadcast_rows_refused_by_tma_families(lib):
+    """Batch and head broadcasts are served by every family; broadcast rows
+    (row stride 0) are refused by the families that read 128-row TMA tiles."""
+    q, k, v = _qkv(B=2, Hq=4, Hkv=2, Sq=320, Skv=320, D=64)
+    kb = k[:1].expand_as(k)
+    assert sm.sdpa_math_plan(q, kb, v, variant="twopass")["variant"] == "twopass"
+    qr = q[:, :, :1].expand_as(q)
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(qr, k, v, variant="twopass"), "broadcast")
+    assert sm.sdpa_math_plan(qr, k, v)["variant"] == "simt"

@@ -35,8 +35,9 @@ def _lib():
 
 def _run(q, k, v, mask, causal, scale, variant="auto", lse=False):
     dev = torch.device("cuda")
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    md = mask.to(dev) if mask is not None else None
+    # device tensors are used as they are (views with broadcast strides included)
+    qd, kd, vd = (t if t.is_cuda else t.to(dev) for t in (q, k, v))
+    md = (mask if mask.is_cuda else mask.to(dev)) if mask is not None else None
     if md is not None:
         while md.dim() < 4:
             md = md.unsqueeze(0)
@@ -239,3 +240,51 @@ def test_forced_unsupported_variant_is_an_error():
     with pytest.raises(sm.SdpaError) as ei:
         _run(q, k, v, None, False, 0.125, variant="twopass")
     assert ei.value.status == sm.SDPA_ERR_UNSUPPORTED
+
+
+# --------------------------------------------------------------------------- broadcast (stride-0) input views
+
+def _broadcast_views(form, q, k, v):
+    """Device views of q, k, v with one dimension broadcast (stride 0)."""
+    dev = torch.device("cuda")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    if form == "kv_batch":      # every batch reads batch 0's keys and values
+        kd, vd = kd[:1].expand_as(kd), vd[:1].expand_as(vd)
+    elif form == "kv_heads":    # every key/value head reads head 0
+        kd, vd = kd[:, :1].expand_as(kd), vd[:, :1].expand_as(vd)
+    elif form == "q_heads":     # every query head reads head 0's queries
+        qd = qd[:, :1].expand_as(qd)
+    elif form == "q_rows":      # every query row is row 0
+        qd = qd[:, :, :1].expand_as(qd)
+    return qd, kd, vd
+
+
+BCAST_SHAPES = [
+    # B, Hq, Hkv, Sq, Skv, D, dtype, causal
+    (2, 4, 2, 200, 264, 128, "f16", False),   # two-pass / paired (TMA), SIMT
+    (2, 4, 2, 130, 200, 64, "bf16", True),    # fused (cp.async), two-pass, SIMT
+    (2, 8, 2, 1, 1152, 128, "f16", False),    # decode, split-KV, tensor-core decode (TMA), SIMT
+]
+
+
+@pytest.mark.parametrize("form", ["kv_batch", "kv_heads", "q_heads", "q_rows"])
+@pytest.mark.parametrize("shape", range(len(BCAST_SHAPES)), ids=lambda i: "x".join(map(str, BCAST_SHAPES[i])))
+def test_broadcast_input_views(shape, form):
+    """Inputs that are expand()ed views (stride 0 over batch, heads or rows)
+    run on every family that accepts them, without a copy, and match the
+    oracle on the materialised inputs.  Families that read 128-row TMA tiles
+    refuse broadcast rows (the plan says so); the others serve every form."""
+    B, Hq, Hkv, Sq, Skv, D, dt, causal = BCAST_SHAPES[shape]
+    q, k, v, _ = W.make_custom(700 + shape, B, Hq, Hkv, Sq, Skv, D, dt)
+    qd, kd, vd = _broadcast_views(form, q, k, v)
+    assert 0 in (qd.stride() + kd.stride() + vd.stride())
+    variants = _variants_for(qd, kd, vd, None, causal)
+    assert "simt" in variants
+    if form == "q_rows":
+        assert not {"twopass", "paired"} & set(variants)
+    qc, kc, vc = (t.contiguous().cpu() for t in (qd, kd, vd))
+    Or, Pr, _ = oracle_fwd(qc, kc, vc, None, is_causal=causal, scale=1.0 / math.sqrt(D), nthreads=NTHREADS)
+    for variant in ["auto"] + variants:
+        O, P, _ = _run(qd, kd, vd, None, causal, 1.0 / math.sqrt(D), variant)
+        compare(O, Or, q.dtype, f"O {form} {variant}", extra=o_allowance(Pr, vc, Hq // Hkv, q.dtype))
+        compare(P, Pr, q.dtype, f"P {form} {variant}")

@@ -32,3 +32,16 @@ def test_wrong_output_fails():
     bad[0, 1, 10, 3] += 0.05
     with pytest.raises(AssertionError):
         compare(bad, O, torch.bfloat16, "O", extra=o_allowance(P, v, 1, torch.bfloat16))
+
+
+def test_f16_is_held_to_the_plain_tolerance():
+    """An f16 O error of 2.5e-3 at a large magnitude fails: f16 and f32 get no
+    ulp or rounded-P allowance, only the plain max-abs bound."""
+    q, k, v, _ = W.make_custom(42, 1, 2, 2, 64, 64, 64, "f16")
+    O, P, _ = oracle_fwd(q, k, v, is_causal=True, scale=0.125)
+    got = torch.from_numpy(O).to(torch.float16).double()
+    i = np.unravel_index(np.argmax(np.abs(O)), O.shape)
+    assert abs(O[i]) > 2.0
+    got[i] = float(O[i]) + 2.5e-3  # exactly 2.5e-3 off
+    with pytest.raises(AssertionError):
+        compare(got, O, torch.float16, "O", extra=o_allowance(P, v, 1, torch.float16))
