@@ -233,6 +233,46 @@ sdpa_status sdpa_math_bwd_ex(const sdpa_tensor *q, const sdpa_tensor *k, const s
                              sdpa_variant variant, sdpa_stream_t stream);
 
 /*
+ * sdpa_math_bwd_noalloc -- sdpa_math_bwd for callers that cannot allocate
+ * device memory.  (The pages have no counterpart of this call; it is an
+ * addition of this library.)
+ *
+ * sdpa_math_bwd needs a B*Hq*Sq float buffer from the caller to carry the
+ * per-row sums from its first kernel to its second.  Some callers cannot
+ * provide one: code hosted inside a framework that hands out all device
+ * memory from its own pre-planned pool and forbids side allocations, or a
+ * real-time path that must not call cudaMalloc after start-up because the
+ * call can block and synchronise the device.  This entry point takes no such
+ * buffer.  It uses a fixed array in the library's own device memory instead
+ * (SDPA_BWD_NOALLOC_MAX_ROWS floats, 4 MiB, held by every GPU that loads the
+ * library until the process exits) and allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * Arguments, semantics, kernels and results are those of sdpa_math_bwd with
+ * an internal rowsum buffer (the per-row sums are not returned).  The caller
+ * still owns q, k, v, probs, dout, dprobs, dq, dk, dv and the stream.
+ *
+ *   - Size limit: B*Hq*Sq (the query rows of q) must not exceed
+ *     SDPA_BWD_NOALLOC_MAX_ROWS; larger calls return SDPA_ERR_UNSUPPORTED
+ *     before anything is enqueued.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (with that device current) and keeps it for later calls; make
+ *     that first call before any stream capture.  A failed look-up returns
+ *     SDPA_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array, and it keeps the
+ *     last call's contents.  Nothing in it needs to start at zero (each call
+ *     writes every row it later reads).  Two calls whose kernels overlap on
+ *     the GPU (for example on two streams without ordering between them)
+ *     race on the array and give wrong gradients: order such calls.
+ * Other errors as sdpa_math_bwd.
+ */
+#define SDPA_BWD_NOALLOC_MAX_ROWS (1 << 20)
+sdpa_status sdpa_math_bwd_noalloc(const sdpa_tensor *q, const sdpa_tensor *k, const sdpa_tensor *v,
+                                  const sdpa_tensor *probs, const sdpa_tensor *dout, const sdpa_tensor *dprobs,
+                                  float scale, sdpa_tensor *dq, sdpa_tensor *dk, sdpa_tensor *dv,
+                                  sdpa_stream_t stream);
+
+/*
  * sdpa_math_selftest_wait -- diagnostic for the failure path above.  Enqueues
  * on `stream` one single-thread kernel that waits, through the same bounded
  * mbarrier wait the tensor-core kernels use, on a barrier nothing ever

@@ -31,6 +31,8 @@ SDPA_OK, SDPA_ERR_INVALID_ARGUMENT, SDPA_ERR_UNSUPPORTED, SDPA_ERR_CUDA, SDPA_ER
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARGUMENT", 2: "SDPA_ERR_UNSUPPORTED",
           3: "SDPA_ERR_CUDA", 4: "SDPA_ERR_TIMEOUT"}
 SDPA_F32, SDPA_F16, SDPA_BF16, SDPA_BOOL = range(4)
+# Query rows (B*Hq*Sq) sdpa_math_bwd_noalloc serves (its fixed device row-sum array).
+SDPA_BWD_NOALLOC_MAX_ROWS = 1 << 20
 MASK_NONE, MASK_BOOL, MASK_ADDITIVE = range(3)
 VARIANTS = {"auto": 0, "simt": 1, "twopass": 2, "fused": 3, "decode": 4, "paired": 5, "split": 6, "tcdecode": 7}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
@@ -99,6 +101,8 @@ def load_library(build_if_missing: bool = False):
         lib.sdpa_math_bwd_ex.restype = ctypes.c_int
         lib.sdpa_math_bwd_ex.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_void_p,
                                          ctypes.c_int, ctypes.c_void_p]
+        lib.sdpa_math_bwd_noalloc.restype = ctypes.c_int
+        lib.sdpa_math_bwd_noalloc.argtypes = [T, T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_void_p]
         lib.sdpa_math_selftest_wait.restype = ctypes.c_int
         lib.sdpa_math_selftest_wait.argtypes = [ctypes.c_void_p]
         lib.sdpa_math_last_error.restype = ctypes.c_char_p
@@ -243,6 +247,21 @@ def sdpa_math_bwd(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, strea
     else:
         code = BWD_VARIANTS[variant] if isinstance(variant, str) else int(variant)
         st = lib.sdpa_math_bwd_ex(*common, code, _stream_handle(stream))
+    if st != SDPA_OK:
+        _raise(lib, st)
+
+
+def sdpa_math_bwd_noalloc(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, stream=None) -> None:
+    """The C-ABI backward that allocates nothing and takes no row-sum buffer
+    (for callers that cannot allocate device memory at call time); the
+    library keeps the per-row sums in its own fixed device array, so at most
+    SDPA_BWD_NOALLOC_MAX_ROWS query rows (B*Hq*Sq) per call.  Raises on error."""
+    lib = load_library()
+    args = [describe(t) for t in (q, k, v, probs, dout)]
+    dg = describe(dprobs) if dprobs is not None else None
+    outs = [describe(t) for t in (dq, dk, dv)]
+    st = lib.sdpa_math_bwd_noalloc(*(ctypes.byref(a) for a in args), ctypes.byref(dg) if dg is not None else None,
+                                   float(scale), *(ctypes.byref(o) for o in outs), _stream_handle(stream))
     if st != SDPA_OK:
         _raise(lib, st)
 

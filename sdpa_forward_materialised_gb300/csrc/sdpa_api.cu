@@ -13,6 +13,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <mutex>
 
 #include "sdpa_math.h"  // include/ is on the compiler search path
 #include "internal.h"
@@ -443,3 +444,63 @@ sdpa_status sdpa_math_selftest_wait(sdpa_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- backward without caller scratch
+// sdpa_math_bwd takes a caller-allocated B*Hq*Sq float buffer for the per-row
+// sums its rows kernel writes and its keys kernel reads.  Callers that cannot
+// allocate device memory at call time (a framework that owns all device
+// memory through its own pre-planned pool, a real-time path that forbids
+// cudaMalloc after start-up) use sdpa_math_bwd_noalloc, which keeps those
+// sums in the fixed array below instead.  It lives in the library's own
+// device memory on every GPU that loads the library, until the process exits.
+// Every call shares it; nothing in it must start at zero, because each call's
+// rows kernel writes every row before its keys kernel reads it.  Calls that
+// overlap on the GPU race on it.
+namespace {
+
+static __device__ __align__(256) float g_bwd_rowsum_scratch[SDPA_BWD_NOALLOC_MAX_ROWS];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices];  // device address of the array, per device (null until looked up)
+
+// Device address of the array on the current device.  In host code the
+// array's name is a host-side stand-in, not a device address, so it is looked
+// up once per device with that device current and cached.
+cudaError_t scratch_address(float** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_bwd_rowsum_scratch);
+        if (e != cudaSuccess) return e;
+        g_scratch_ptr[dev] = static_cast<float*>(p);
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" sdpa_status sdpa_math_bwd_noalloc(const sdpa_tensor* q, const sdpa_tensor* k, const sdpa_tensor* v,
+                                             const sdpa_tensor* probs, const sdpa_tensor* dout,
+                                             const sdpa_tensor* dprobs, float scale, sdpa_tensor* dq,
+                                             sdpa_tensor* dk, sdpa_tensor* dv, sdpa_stream_t stream) {
+    g_last_error.clear();
+    sdpa_status s = check_tensor(q, "q");
+    if (s != SDPA_OK) return s;
+    const int64_t rows = q->shape[0] * q->shape[1] * q->shape[2];
+    if (rows > (int64_t)SDPA_BWD_NOALLOC_MAX_ROWS)
+        return fail(SDPA_ERR_UNSUPPORTED,
+                    "sdpa_math_bwd_noalloc serves at most %lld query rows (B*Hq*Sq), got %lld; "
+                    "use sdpa_math_bwd with a caller buffer",
+                    (long long)SDPA_BWD_NOALLOC_MAX_ROWS, (long long)rows);
+    float* rowsum = nullptr;
+    const cudaError_t e = scratch_address(&rowsum);
+    if (e != cudaSuccess)
+        return fail(SDPA_ERR_CUDA, "looking up the library's row-sum array failed: %s", cudaGetErrorString(e));
+    return sdpa_math_bwd_ex(q, k, v, probs, dout, dprobs, scale, dq, dk, dv, rowsum, SDPA_VARIANT_AUTO, stream);
+}

@@ -335,6 +335,18 @@ def test_empty_value_head_dim_with_aligned_rows_plans_without_crashing(lib):
         _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant=forced))
 
 
+def test_noalloc_backward_rejects_more_rows_than_its_array(lib):
+    """sdpa_math_bwd_noalloc refuses, on the host and before any CUDA call,
+    a call with more query rows (B*Hq*Sq) than its fixed row-sum array holds."""
+    rows = sm.SDPA_BWD_NOALLOC_MAX_ROWS + 1
+    q = torch.zeros(1, 1, rows, 1, dtype=torch.float16)
+    k = torch.zeros(1, 1, 4, 1, dtype=torch.float16)
+    P = torch.zeros(1, 1, rows, 4, dtype=torch.float16)
+    _expect("SDPA_ERR_UNSUPPORTED",
+            lambda: sm.sdpa_math_bwd_noalloc(q, k, k, P, q, None, 1.0, torch.empty_like(q), torch.empty_like(k),
+                                             torch.empty_like(k), stream=0), "at most")
+
+
 def test_outputs_must_not_overlap_themselves(lib):
     """An out or probs view with stride 0 over more than one element would be
     written by several threads at once: refused on the host."""
