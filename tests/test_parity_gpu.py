@@ -275,6 +275,8 @@ def test_broadcast_input_views(shape, form):
     oracle on the materialised inputs.  Families that read 128-row TMA tiles
     refuse broadcast rows (the plan says so); the others serve every form."""
     B, Hq, Hkv, Sq, Skv, D, dt, causal = BCAST_SHAPES[shape]
+    if form == "q_rows" and Sq == 1:
+        pytest.skip("a single query row has nothing to broadcast")
     q, k, v, _ = W.make_custom(700 + shape, B, Hq, Hkv, Sq, Skv, D, dt)
     qd, kd, vd = _broadcast_views(form, q, k, v)
     assert 0 in (qd.stride() + kd.stride() + vd.stride())
