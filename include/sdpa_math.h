@@ -164,7 +164,8 @@ typedef struct {
  * TC_DECODE (D = Dv = 128, f16/bf16), else SPLIT; otherwise the tensor-core
  * families, chosen by the number of score tiles that survive causal truncation
  * rather than by area (the page's fusion criterion, "single-kernel fusion
- * (small shapes)" update): TC_FUSED up to 256 keys, then TC_PAIRED (two query
+ * (small shapes)" update): TC_FUSED while every 128-row block keeps at most
+ * two live 128-key tiles (Skv <= 256, or causal with Sq <= 256), then TC_PAIRED (two query
  * tiles per CTA) for calls without a causal mask when the paired grid still
  * gives about one CTA per SM, else TC_TWOPASS; SIMT when none accepts the
  * layout.  `requested` is the variant the caller would pass to

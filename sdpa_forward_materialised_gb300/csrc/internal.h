@@ -41,6 +41,16 @@ inline int64_t live_tiles_per_slice(int64_t Sq, int64_t Skv, bool causal) {
     return n;
 }
 
+// Live 128-key tiles of the row block that keeps the most of them (the last
+// one) after top-left causal truncation: every row block of a call has at most
+// this many key tiles with a visible key.
+inline int64_t max_live_key_tiles(int64_t Sq, int64_t Skv, bool causal) {
+    if (Sq <= 0 || Skv <= 0) return 0;
+    if (!causal) return (Skv + 127) / 128;
+    const int64_t last = (Sq - 1 < Skv - 1 ? Sq - 1 : Skv - 1);
+    return last / 128 + 1;
+}
+
 // The backward's validated arguments (element strides for [B, H, S] of every
 // tensor; the innermost stride is 1).  dprobs may be null (no gradient through
 // P); rowsum is the caller's B*Hq*Sq float buffer for sum_j P dP per row.

@@ -1,7 +1,7 @@
 // sdpa_tc.cu -- tcgen05 tensor-core kernels of the materialised-probability
 // SDPA forward (fp16 / bf16, head dim 64 or 128, positive scale): the
 // two-pass kernel (one or two 128-row query tiles per CTA) and the fused
-// single-sweep kernel for at most 256 keys.
+// single-sweep kernel for row blocks with at most two live 128-key tiles.
 //
 // What they compute: FlagOS-OP PR #10 "feat: add sdpa_math operator" -- the
 // math backend's (out, attn_probs): P = softmax(scale*QK^T + mask), O = P V,
@@ -764,12 +764,335 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- two-pass kernel, 256-key score tiles
+// One 128-row query tile per CTA (causal calls, and grids the paired layout
+// cannot fill).  Q K^T runs over pairs of key tiles as 128 x 256 x 16 MMAs
+// with Q in TMEM as the A operand: on GB300 such an instruction takes ~137
+// cycles against ~107 for a 128 x 128 x 16 one with both operands in shared
+// memory, so the score products of both sweeps cost about 0.64x of the
+// 128-key form.  P V stays 128 x D x 16 with P from the worker's shared tile.
+//
+// TMEM (512 columns): S of a key-tile pair in [0, 256) (worker w reads
+// [128 w, 128 w + 128)), O in [256, 256 + D), Q in [384, 384 + D / 2) as
+// packed element pairs.  Shared memory: a ring of pair slots (two K tiles laid
+// out as one 256-row operand, chunk c of tile t at c * 32 KB + t * 16 KB; or
+// two V tiles one after the other) and one P tile per worker; P tile 0 holds
+// the Q tile until worker 0 has copied it into TMEM.
+//   warp 0       TMA producer: Q, K pairs (sweep 1), then K pairs and V pairs
+//   warp 1       TMEM allocator + MMA issuer
+//   warps 2, 3   zero-fill of P above the causal diagonal
+//   warps 4..11  two softmax workers; worker w takes key tile 2 p + w of pair p
+template <int D>
+struct WideCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTile = 128 * D * 2;      // one 128-row Q / K / V tile
+    static constexpr int kSlot = 2 * kTile;        // a pair of K or V tiles
+    static constexpr int kPBytes = 128 * 128 * 2;  // one P tile
+    static constexpr int kBarBytes = 256;
+    static constexpr int kMaxSmem = 227 * 1024;
+    static constexpr int kFree = kMaxSmem - 2 * kPBytes - kBarBytes - 1024;
+    static constexpr int kSlots = kFree / kSlot > 6 ? 6 : kFree / kSlot;
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffP = kSlots * kSlot;
+    static constexpr int kOffBar = kOffP + 2 * kPBytes;
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kColS = 0, kColO = 256, kColQ = 384;
+    static constexpr int bQ = 0;             // Q tile landed in P tile 0 (TMA)
+    static constexpr int bQT = 1;            // Q in TMEM (128 arrivals)
+    static constexpr int bF = 2;             // [kSlots] slot full (TMA)
+    static constexpr int bE = bF + kSlots;   // [kSlots] slot consumed (MMA commit)
+    static constexpr int bSF = bE + kSlots;  // S full (MMA commit)
+    static constexpr int bSE = bSF + 1;      // S read out by both workers (256 arrivals)
+    static constexpr int bPF = bSE + 1;      // [2] P tile full (128 arrivals)
+    static constexpr int bPV = bPF + 2;      // [2] P tile consumed by P V (MMA commit)
+    static constexpr int bO = bPV + 2;       // O complete (MMA commit)
+    static constexpr int kBars = bO + 1;
+    static_assert(kBars * 8 + 16 <= kBarBytes, "barrier block");
+    static_assert(kSlots >= 2, "ring too shallow");
+    static_assert(kSmem <= kMaxSmem, "shared memory budget");
+    static_assert(kColO + D <= kColQ && kColQ + D / 2 <= 512, "TMEM budget");
+};
+
+template <int D, typename T, bool kMasked>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_p,
+               const __grid_constant__ CUtensorMap tm_o, const TcParams prm) {
+    using C = WideCfg<D>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sRing = smem_u32(smem + C::kOffRing);
+    const uint32_t sP = smem_u32(smem + C::kOffP);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int hk = h / prm.group;
+    const int qt = prm.n_qtiles - 1 - (int)blockIdx.z;  // heaviest causal tiles first
+    const int r0 = qt * 128;
+    const int n = live_tiles(prm, qt);                  // live key tiles
+    const int np = (n + 1) / 2;                         // key-tile pairs
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kBars; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(C::bQT), 128);
+        mbar_init(bar(C::bSE), 256);
+        mbar_init(bar(C::bPF), 128);
+        mbar_init(bar(C::bPF + 1), 128);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {  // producer / MMA / zero-fill warpgroup
+        setmaxnreg_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            mbar_arrive_expect_tx(bar(C::bQ), C::kTile);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sP + c * 16384, &tm_q, bar(C::bQ), c * 64, pick(prm.ord_q & 3, r0, h, b),
+                            pick((prm.ord_q >> 2) & 3, r0, h, b), pick((prm.ord_q >> 4) & 3, r0, h, b));
+            int it = 0;
+            auto load_pair = [&](const CUtensorMap* tm, uint32_t ord, int p, bool is_k) {
+                const int s = it % C::kSlots;
+                wait_bar(bar(C::bE + s), ((it / C::kSlots) & 1) ^ 1, abort_flag, 1, C::bE + s);
+                const int nt = min(2, n - 2 * p);
+                mbar_arrive_expect_tx(bar(C::bF + s), nt * C::kTile);
+                for (int t = 0; t < nt; ++t) {
+                    const int kv0 = (2 * p + t) * 128;
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(sRing + s * C::kSlot + (is_k ? c * 32768 + t * 16384 : t * C::kTile + c * 16384),
+                                    tm, bar(C::bF + s), c * 64, pick(ord & 3, kv0, hk, b),
+                                    pick((ord >> 2) & 3, kv0, hk, b), pick((ord >> 4) & 3, kv0, hk, b));
+                }
+                ++it;
+            };
+            // the MMA issuer consumes: K pairs 0..np-1 (sweep 1); then K pair 0 and,
+            // for each pair p, K pair p+1 (when it exists) followed by V pair p
+            for (int p = 0; p < np; ++p) load_pair(&tm_k, prm.ord_k, p, true);
+            load_pair(&tm_k, prm.ord_k, 0, true);
+            for (int p = 0; p < np; ++p) {
+                if (p + 1 < np) load_pair(&tm_k, prm.ord_k, p + 1, true);
+                load_pair(&tm_v, prm.ord_v, p, false);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc_qk2 = idesc_f16(128, 256, kBF16, false);
+            constexpr uint32_t idesc_qk1 = idesc_f16(128, 128, kBF16, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
+            // descriptor bases: a slot, tile or K step adds its byte offset / 16
+            // to the start-address field (addresses stay below 2^18 bytes)
+            const uint64_t kdesc0 = sw128_desc(sRing, 16, 1024);
+            const uint64_t vdesc0 = sw128_desc(sRing, 16384, 1024);
+            const uint64_t pdesc0 = sw128_desc(sP, 16, 1024);
+            wait_bar(bar(C::bQT), 0, abort_flag, 2, C::bQT);
+            tc_fence_after();
+            int it = 0, s_use = 0, pu0 = 0, pu1 = 0;
+            bool o_init = false;
+            // S = Q [K_2p | K_2p+1]^T (N = 256, or 128 for a lone last tile)
+            auto qk = [&](int p) {
+                const int s = it % C::kSlots;
+                wait_bar(bar(C::bF + s), (it / C::kSlots) & 1, abort_flag, 2, C::bF + s);
+                wait_bar(bar(C::bSE), (s_use & 1) ^ 1, abort_flag, 2, C::bSE);
+                tc_fence_after();
+                const uint64_t kd = kdesc0 + static_cast<uint64_t>((s * C::kSlot) >> 4);
+                const uint32_t idesc = (2 * p + 1 < n) ? idesc_qk2 : idesc_qk1;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_f16_ts(tmem + C::kColS, tmem + C::kColQ + kk * 8,
+                                  kd + static_cast<uint64_t>(((kk / 4) * 32768 + (kk % 4) * 32) >> 4), idesc,
+                                  kk > 0 ? 1u : 0u);
+                tc_commit(bar(C::bSF));
+                tc_commit(bar(C::bE + s));
+                ++it;
+                ++s_use;
+            };
+            // O += P_t V_t for the tiles of pair p, P from worker t's tile
+            auto pv = [&](int p) {
+                const int s = it % C::kSlots;
+                wait_bar(bar(C::bF + s), (it / C::kSlots) & 1, abort_flag, 2, C::bF + s);
+                const int nt = min(2, n - 2 * p);
+                for (int t = 0; t < nt; ++t) {
+                    wait_bar(bar(C::bPF + t), (t ? pu1 : pu0) & 1, abort_flag, 2, C::bPF + t);
+                    tc_fence_after();
+                    const uint64_t vd = vdesc0 + static_cast<uint64_t>((s * C::kSlot + t * C::kTile) >> 4);
+                    const uint64_t pd = pdesc0 + static_cast<uint64_t>((t * C::kPBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_f16(tmem + C::kColO, pd + static_cast<uint64_t>(((kk / 4) * 16384 + (kk % 4) * 32) >> 4),
+                                   vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (o_init || kk > 0) ? 1u : 0u);
+                    o_init = true;
+                    tc_commit(bar(C::bPV + t));
+                    if (t) ++pu1;
+                    else ++pu0;
+                }
+                tc_commit(bar(C::bE + s));
+                ++it;
+            };
+            // sweep 1, then sweep 2 with the next pair's Q K^T ahead of this pair's P V
+            for (int p = 0; p < np; ++p) qk(p);
+            qk(0);
+            for (int p = 0; p < np; ++p) {
+                if (p + 1 < np) qk(p + 1);
+                pv(p);
+            }
+            tc_commit(bar(C::bO));
+        } else if (warp >= 2) {
+            // ------------------------------------------------------------ causal zero tiles
+            zero_p_region(prm, b, h, r0, min(r0 + 128, prm.Sq), n * 128, warp - 2, 2, lane);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax workers
+        setmaxnreg_inc<kRegsHigh>();
+        const int w = (warp - 4) >> 2;
+        const int t = (threadIdx.x - 128) & 127;  // row within the tile == TMEM lane
+        const int row = r0 + t;
+        const bool row_ok = row < prm.Sq;
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_tmem = tmem + lane_base + C::kColS + w * 128;
+        const float cexp = kMasked ? 1.f : prm.c2;
+
+        // Q into TMEM (worker 0): row t of the swizzled tile in P tile 0, as
+        // packed element pairs in columns [kColQ, kColQ + D / 2) of lane t
+        if (w == 0) {
+            wait_bar(bar(C::bQ), 0, abort_flag, 3, C::bQ);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c) {
+                uint32_t qr[32];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const uint4 v4 = ld_shared_v4(sP + c * 16384 + t * 128 + ((u ^ (t % 8)) * 16));
+                    qr[4 * u] = v4.x;
+                    qr[4 * u + 1] = v4.y;
+                    qr[4 * u + 2] = v4.z;
+                    qr[4 * u + 3] = v4.w;
+                }
+                tmem_st32(tmem + lane_base + C::kColQ + c * 32, qr);
+            }
+            tc_fence_before();
+            mbar_arrive(bar(C::bQT));
+        }
+
+        float s[128];
+        int s_use = 0;
+        // every pair's S: both workers wait for it and release it, in step
+        auto load_s = [&](bool has, int role) {
+            wait_bar(bar(C::bSF), s_use & 1, abort_flag, role, C::bSF);
+            tc_fence_after();
+            if (has) tmem_ld128(s_tmem, s);
+            tc_fence_before();
+            mbar_arrive(bar(C::bSE));
+            ++s_use;
+        };
+
+        // sweep 1: this worker's tiles -> partial row max / sum of exp2
+        float m = -CUDART_INF_F, l = 0.f;
+        for (int p = 0; p < np; ++p) {
+            const int j = 2 * p + w;
+            const bool has = j < n;
+            load_s(has, 4);
+            if (has) {
+                mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+                tile_stats(s, cexp, m, l);
+            }
+        }
+        // merge the two workers' statistics through P tile 1 (idle until
+        // sweep 2): both combine the same values in the same order, so they
+        // hold bit-identical lse per row
+        float* xs = reinterpret_cast<float*>(smem + C::kOffP + C::kPBytes);  // [worker][m, l][128]
+        xs[(w * 2 + 0) * 128 + t] = m;
+        xs[(w * 2 + 1) * 128 + t] = l;
+        softmax_group_sync();
+        float lse2;
+        {
+            const float a0 = xs[t], b0 = xs[128 + t], a1 = xs[256 + t], b1 = xs[384 + t];
+            const float mm = fmaxf(a0, a1);
+            lse2 = (mm == -CUDART_INF_F) ? -CUDART_INF_F : mm + log2f(b0 * ex2(a0 - mm) + b1 * ex2(a1 - mm));
+        }
+        softmax_group_sync();  // both read the exchange before any P tile is written
+        if (lane == 0) {
+            prefetch_tmap(&tm_p);
+            prefetch_tmap(&tm_o);
+        }
+        const bool dead = lse2 == -CUDART_INF_F;
+        const float neg = dead ? -CUDART_INF_F : -lse2;  // a dead row adds -inf: every p is 0
+
+        // sweep 2: exact P of this worker's tiles into its swizzled P tile, then TMA stores
+        int p_use = 0;
+        for (int p = 0; p < np; ++p) {
+            const int j = 2 * p + w;
+            const bool has = j < n;
+            load_s(has, 5);
+            if (!has) continue;
+            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, j * 128);
+            uint32_t hp[64];
+            tile_probs<T>(s, cexp, neg, hp);
+            wait_bar(bar(C::bPV + w), (p_use & 1) ^ 1, abort_flag, 5, C::bPV + w);
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            store_p_row(hp, sP + w * C::kPBytes, t);
+            fence_proxy_async_smem();
+            mbar_arrive(bar(C::bPF + w));
+            __syncwarp();
+            if (lane == 0) warp_store_p(&tm_p, prm.ord_p, sP + w * C::kPBytes, warp & 3, j * 128, r0, h, b);
+            ++p_use;
+        }
+        if (lane == 0) bulk_wait0();  // the P tile is read out before O reuses it
+        __syncwarp();
+
+        // epilogue: worker w stages and stores the 64-column chunk w of O
+        // (D = 128), or worker 0 all of it (D = 64), through its idle P tile
+        wait_bar(bar(C::bO), 0, abort_flag, 6, C::bO);
+        tc_fence_after();
+        if (D == 128 || w == 0) {
+            const int c0 = D == 128 ? w : 0;
+            const uint32_t obuf = sP + w * C::kPBytes;
+            stage_o_row<T, 1>(tmem + lane_base + C::kColO + 64 * c0, obuf, t, dead);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) warp_store_o<1>(&tm_o, prm.ord_o, obuf, warp & 3, 64 * c0, r0, h, b);
+            if (lane == 0) bulk_wait0();
+        }
+        if (w == 0 && prm.lse && row_ok)
+            prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        if (*abort_flag) {
+            // give in-flight TMA / tcgen05 work time to land before freeing TMEM
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        }
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 // ---------------------------------------------------------------- fused single-sweep kernel
-// Small key counts (Skv <= 256: at most two 128-key score tiles per row
-// block): S for every key of the row block stays in TMEM, so the row max, the
-// sum of exponentials and P = exp(S - lse) all come from one Q K^T, and the
-// whole forward is one launch with no second sweep (the small-shape fused
-// variant of the page's "single-kernel fusion (small shapes)" update).
+// Row blocks with at most two live 128-key score tiles (Skv <= 256, or a
+// causal mask over at most 256 query rows): S for every live key of the row
+// block stays in TMEM, so the row max, the sum of exponentials and
+// P = exp(S - lse) all come from one Q K^T, and the whole forward is one
+// launch with no second sweep (the small-shape fused variant of the page's
+// "single-kernel fusion (small shapes)" update, which counts tiles after
+// causal truncation).  Keys past the live tiles get P = 0.
 //
 // One CTA (256 threads, two warpgroups) per 128-row query tile of one
 // (batch, head).  Q, K and V arrive by asynchronous 16-byte copies straight in
@@ -848,8 +1171,13 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     const int h = blockIdx.x, b = blockIdx.y, qt = blockIdx.z;
     const int hk = h / prm.group;
     const int r0 = qt * 128;
-    const int n_kv = (prm.Skv + 127) / 128;  // 1 or 2
-    const uint32_t kTmemO = n_kv * 128;      // O columns follow the S tiles
+    // live key tiles of this row block (1 or 2): with a causal mask the keys
+    // past its last row are masked for every row, so they are never computed
+    // and their P columns are written as zeros
+    int n_kv = (prm.Skv + 127) / 128;
+    if (prm.causal) n_kv = min(n_kv, min(min(r0 + 127, prm.Sq - 1), prm.Skv - 1) / 128 + 1);
+    const int live_end = min(prm.Skv, n_kv * 128);  // keys [live_end, Skv) have P = 0 in every row
+    const uint32_t kTmemO = n_kv * 128;             // O columns follow the S tiles
 
     if (threadIdx.x == 0) {
         mbar_init(smem_u32(&bars[0]), 1);
@@ -1030,17 +1358,18 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
                 return sP + (key >> 7) * (128 * 128 * 2) + (kt >> 6) * 16384 + rr * 128 +
                        ((((kt >> 3) & 7) ^ (rr & 7)) << 4) + (kt & 7) * 2;
             };
+            // (live_end is a multiple of 128 or Skv, so a key pair never straddles it)
             if ((reinterpret_cast<uintptr_t>(prow) & 3) == 0) {
                 for (int key = 2 * lane; key < prm.Skv; key += 64) {
-                    uint32_t v;
-                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src(key)));
+                    uint32_t v = 0;
+                    if (key < live_end) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src(key)));
                     if (key + 1 < prm.Skv) *reinterpret_cast<uint32_t*>(prow + key) = v;
                     else prow[key] = static_cast<uint16_t>(v);
                 }
             } else {
                 for (int key = lane; key < prm.Skv; key += 32) {
-                    uint16_t v;
-                    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(src(key)));
+                    uint16_t v = 0;
+                    if (key < live_end) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(src(key)));
                     prow[key] = v;
                 }
             }
@@ -2074,6 +2403,42 @@ cudaError_t launch_twopass(const Problem& p, cudaStream_t stream) {
 }
 
 template <int D, typename T, bool kMasked>
+cudaError_t launch_wide(const Problem& p, cudaStream_t stream) {
+    using C = WideCfg<D>;
+    CUtensorMap mq, mk, mv, mp, mo;
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    if (!make_map(&mq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, 128, &prm.ord_q) ||
+        !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, 128, &prm.ord_k) ||
+        !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 128, &prm.ord_v) ||
+        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 32, &prm.ord_p) ||
+        !make_map(&mo, p.dtype, p.o, p.Dv, p.Sq, p.Hq, p.B, p.so, 32, &prm.ord_o))
+        return cudaErrorNotSupported;
+    prm.Sq = (int)p.Sq;
+    prm.Skv = (int)p.Skv;
+    prm.Hq = (int)p.Hq;
+    prm.group = (int)p.group;
+    prm.n_qtiles = (int)((p.Sq + 127) / 128);
+    prm.causal = p.causal;
+    prm.c2 = p.scale * kLog2e;
+    prm.mask = p.mask;
+    prm.mask_kind = p.mask_kind;
+    prm.mask_dtype = p.mask_dtype;
+    prm.sm0 = p.sm[0]; prm.sm1 = p.sm[1]; prm.sm2 = p.sm[2];
+    prm.o = p.o;
+    prm.so0 = p.so[0]; prm.so1 = p.so[1]; prm.so2 = p.so[2];
+    prm.lse = p.lse;
+    prm.p = p.p;
+    prm.sp0 = p.sp[0]; prm.sp1 = p.sp[1]; prm.sp2 = p.sp[2];
+    auto kern = tc_wide_kernel<D, T, kMasked>;
+    cudaError_t e = prepare_kernel(kern, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)prm.n_qtiles);
+    kern<<<grid, kThreads, C::kSmem, stream>>>(mq, mk, mv, mp, mo, prm);
+    return cudaGetLastError();
+}
+
+template <int D, typename T, bool kMasked>
 cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
     using L = FusedSmem<D>;
     TcParams prm;
@@ -2099,7 +2464,7 @@ cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
     io.q = p.q; io.sq0 = p.sq[0]; io.sq1 = p.sq[1]; io.sq2 = p.sq[2];
     io.k = p.k; io.sk0 = p.sk[0]; io.sk1 = p.sk[1]; io.sk2 = p.sk[2];
     io.v = p.v; io.sv0 = p.sv[0]; io.sv1 = p.sv[1]; io.sv2 = p.sv[2];
-    const uint32_t need = (uint32_t)((p.Skv + 127) / 128 * 128 + D);
+    const uint32_t need = (uint32_t)(max_live_key_tiles(p.Sq, p.Skv, p.causal != 0) * 128 + D);
     io.tmem_cols = need <= 256 ? 256u : 512u;
     auto kern = tc_fused_kernel<D, T, kMasked>;
     cudaError_t e = prepare_kernel(kern, L::kSmem, false);
@@ -2138,6 +2503,10 @@ namespace {
 template <typename T, int QT>
 cudaError_t launch_qt(const Problem& p, cudaStream_t stream) {
     const bool masked = p.mask_kind != kMaskNone;
+    if constexpr (QT == 1) {
+        if (p.D == 64) return masked ? launch_wide<64, T, true>(p, stream) : launch_wide<64, T, false>(p, stream);
+        return masked ? launch_wide<128, T, true>(p, stream) : launch_wide<128, T, false>(p, stream);
+    }
     if (p.D == 64)
         return masked ? launch_twopass<64, T, true, QT>(p, stream) : launch_twopass<64, T, false, QT>(p, stream);
     return masked ? launch_twopass<128, T, true, QT>(p, stream) : launch_twopass<128, T, false, QT>(p, stream);
@@ -2167,7 +2536,9 @@ bool tc_supports(const Problem& p, bool fused, const char** why) {
     if (fused) {
         // plain 16-byte loads of q / k / v rows and stores of O rows; P rows
         // may have any alignment
-        if (p.Skv > 256) { *why = "the fused kernel keeps at most 256 keys in TMEM"; return false; }
+        if (max_live_key_tiles(p.Sq, p.Skv, p.causal != 0) > 2) {
+            *why = "the fused kernel keeps at most two live 128-key tiles per row block in TMEM"; return false;
+        }
         if (!aligned16(p.q) || !aligned16(p.k) || !aligned16(p.v) || !aligned16(p.o)) {
             *why = "q, k, v and out must be 16-byte aligned"; return false;
         }

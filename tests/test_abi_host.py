@@ -198,7 +198,7 @@ def test_f32_always_plans_simt(lib):
 
 
 # AUTO's kernel family per benchmark workload (host-only planning): the fused
-# single-sweep kernel for Skv <= 256, the cluster decode kernel for few rows
+# single-sweep kernel for at most two live key tiles per row block, the cluster decode kernel for few rows
 # per KV head, the tensor-core split-KV kernel when those rows meet a long key
 # sequence at D = 128 (the CUDA-core split-KV kernel at other head dims),
 # the one-tile two-pass kernel under a causal mask, the paired layout for the
@@ -219,11 +219,25 @@ def test_auto_choice_per_workload(lib, name, expect):
     assert sm.sdpa_math_plan(q, k, v, m, is_causal=w.is_causal)["variant"] == expect
 
 
-def test_fused_needs_at_most_256_keys(lib):
+def test_fused_takes_at_most_two_live_key_tiles_per_row_block(lib):
+    """The fused kernel can serve a call when every row block keeps at most two
+    live 128-key tiles after causal truncation (counted tiles, not Skv).  AUTO
+    prefers the two-pass kernels wherever TMA describes the P rows (they
+    measured faster on GB300) and takes the fused kernel for the rest."""
     q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=256, D=64)
+    assert sm.sdpa_math_plan(q, k, v)["variant"] == "twopass"
+    assert sm.sdpa_math_plan(q, k, v, variant="fused")["variant"] == "fused"
+    q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=100, D=64)       # 200-byte P rows: no TMA
     assert sm.sdpa_math_plan(q, k, v)["variant"] == "fused"
     q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=100, Skv=264, D=64)
-    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant="fused"), "256 keys")
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, variant="fused"), "two live")
+    # causal: 256 query rows see at most keys 0..255 whatever Skv is
+    q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=256, Skv=5001, D=64)
+    r = sm.sdpa_math_plan(q, k, v, is_causal=True)
+    assert r["variant"] == "fused" and r["live_score_tiles"] == 2 * 3
+    q, k, v = _qkv(B=1, Hq=2, Hkv=2, Sq=257, Skv=5001, D=64)
+    assert sm.sdpa_math_plan(q, k, v, is_causal=True)["variant"] == "simt"
+    _expect("SDPA_ERR_UNSUPPORTED", lambda: sm.sdpa_math_plan(q, k, v, is_causal=True, variant="fused"), "two live")
 
 
 def test_split_kv_limits(lib):

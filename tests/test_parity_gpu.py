@@ -138,6 +138,12 @@ SMALL = [
     (1, 2, 2, 100, 100, 64, "bf16", False, "bool"),
     (1, 2, 1, 7, 1, 64, "f16", False, None),
     (1, 3, 3, 250, 129, 128, "bf16", False, "additive"),
+    # causal calls whose row blocks keep at most two live key tiles however
+    # long the key sequence (the fused kernel writes the masked tail of P as
+    # zeros), incl. a P row of odd length
+    (1, 4, 2, 200, 1000, 128, "f16", True, None),
+    (2, 2, 2, 256, 300, 64, "bf16", True, None),
+    (1, 2, 1, 130, 1001, 64, "f16", True, None),
     # few rows per KV head over long key sequences (split-KV): ragged chunks
     # and V sub-tiles, masks with fully masked rows, causal rows that see one
     # key, 16 rows at D = 256, and fewer keys than CTAs in the cluster
