@@ -667,7 +667,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="prefill2k_d128_f16", choices=sorted(W.BY_NAME))
     ap.add_argument("--variant", default="auto",
-                    choices=["auto", "simt", "twopass", "paired", "fused", "decode", "split", "tcdecode"])
+                    choices=["auto", "simt", "twopass", "paired", "fused", "onesweep", "decode", "split", "tcdecode"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",

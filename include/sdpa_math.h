@@ -91,8 +91,12 @@ typedef enum {
     SDPA_VARIANT_TC_PAIRED = 5,  /* TC_TWOPASS with two query tiles per CTA sharing each K/V load */
     SDPA_VARIANT_SPLIT = 6,      /* few query rows, long key sequence: keys split over a cluster of up
                                     to 16 CTAs, scores kept on chip, V streamed (split-KV) */
-    SDPA_VARIANT_TC_DECODE = 7   /* few query rows, D = Dv = 128, f16/bf16: the cluster split of SPLIT
+    SDPA_VARIANT_TC_DECODE = 7,  /* few query rows, D = Dv = 128, f16/bf16: the cluster split of SPLIT
                                     with S^T = K Q^T and O^T = V^T P^T on the tensor cores, K / V by TMA */
+    SDPA_VARIANT_TC_ONESWEEP = 8 /* tcgen05, one Q K^T sweep: the live key tiles of a 128-row block
+                                    split over a cluster of up to 8 CTAs (4 tiles each, so at most
+                                    32 tiles = 4096 keys per row block), exp2(S - tile max) kept in
+                                    shared memory, row LSE by DSMEM, then P = that * exp2(max - lse) */
 } sdpa_variant;
 
 typedef struct {

@@ -34,7 +34,8 @@ SDPA_F32, SDPA_F16, SDPA_BF16, SDPA_BOOL = range(4)
 # Query rows (B*Hq*Sq) sdpa_math_bwd_noalloc serves (its fixed device row-sum array).
 SDPA_BWD_NOALLOC_MAX_ROWS = 1 << 20
 MASK_NONE, MASK_BOOL, MASK_ADDITIVE = range(3)
-VARIANTS = {"auto": 0, "simt": 1, "twopass": 2, "fused": 3, "decode": 4, "paired": 5, "split": 6, "tcdecode": 7}
+VARIANTS = {"auto": 0, "simt": 1, "twopass": 2, "fused": 3, "decode": 4, "paired": 5, "split": 6, "tcdecode": 7,
+            "onesweep": 8}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 

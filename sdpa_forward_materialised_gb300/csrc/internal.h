@@ -76,8 +76,9 @@ struct BwdProblem {
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 bool tc_supports(const Problem& p, bool fused, const char** why);
 // mode 1: two-pass kernel, one 128-row query tile per CTA; 2: two-pass kernel,
-// two query tiles per CTA; 3: fused single-sweep kernel.
+// two query tiles per CTA; 3: fused single-sweep kernel; 4: one-sweep cluster kernel.
 cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream);
+bool onesweep_supports(const Problem& p, const char** why);
 // Query tiles per CTA that suit the two-pass kernel for p (1 or 2).
 int tc_query_tiles(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);

@@ -44,6 +44,7 @@ sdpa_variant env_variant() {
         if (!std::strcmp(e, "decode")) return SDPA_VARIANT_DECODE;
         if (!std::strcmp(e, "split")) return SDPA_VARIANT_SPLIT;
         if (!std::strcmp(e, "tcdecode")) return SDPA_VARIANT_TC_DECODE;
+        if (!std::strcmp(e, "onesweep")) return SDPA_VARIANT_TC_ONESWEEP;
         return SDPA_VARIANT_AUTO;
     }();
     return v;
@@ -257,6 +258,11 @@ sdpa_status resolve(const sdpa::Problem& p, sdpa_variant requested, sdpa_variant
                 return fail(SDPA_ERR_UNSUPPORTED, "split variant cannot serve this call: %s", why);
             *out = v;
             return SDPA_OK;
+        case SDPA_VARIANT_TC_ONESWEEP:
+            if (!sdpa::onesweep_supports(p, &why))
+                return fail(SDPA_ERR_UNSUPPORTED, "one-sweep variant cannot serve this call: %s", why);
+            *out = v;
+            return SDPA_OK;
         case SDPA_VARIANT_TC_DECODE:
             if (!sdpa::tc_decode_supports(p, &why))
                 return fail(SDPA_ERR_UNSUPPORTED, "tensor-core decode variant cannot serve this call: %s", why);
@@ -313,6 +319,7 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
         case SDPA_VARIANT_TC_TWOPASS: e = sdpa::launch_tc(p, 1, st); break;
         case SDPA_VARIANT_TC_PAIRED: e = sdpa::launch_tc(p, 2, st); break;
         case SDPA_VARIANT_TC_FUSED: e = sdpa::launch_tc(p, 3, st); break;
+        case SDPA_VARIANT_TC_ONESWEEP: e = sdpa::launch_tc(p, 4, st); break;
         case SDPA_VARIANT_DECODE: e = sdpa::launch_decode(p, st); break;
         case SDPA_VARIANT_SPLIT: e = sdpa::launch_split(p, st); break;
         case SDPA_VARIANT_TC_DECODE: e = sdpa::launch_tc_decode(p, st); break;
@@ -333,7 +340,12 @@ sdpa_status sdpa_math_fwd_ex(const sdpa_tensor* q, const sdpa_tensor* k, const s
                         "chunk too large for shared memory");
         const char* why = nullptr;
         if (chosen == SDPA_VARIANT_TC_DECODE && sdpa::split_supports(p, &why)) e = sdpa::launch_split(p, st);
+        else if (chosen == SDPA_VARIANT_TC_ONESWEEP) e = sdpa::launch_tc(p, 1, st);
         else e = sdpa::launch_simt(p, st);
+        if (e == cudaErrorNotSupported) {
+            (void)cudaGetLastError();
+            e = sdpa::launch_simt(p, st);
+        }
     }
     if (e != cudaSuccess)
         return fail(SDPA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

@@ -41,6 +41,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <type_traits>
@@ -77,6 +78,7 @@ __device__ __forceinline__ int pick(uint32_t sel, int rows, int head, int batch)
 
 struct TcParams {
     int Sq, Skv, Hq, group, n_qtiles, causal;
+    int B, cl;  // batch; CTAs per cluster (one-sweep kernel)
     float c2;  // scale * log2(e), > 0
     const void* mask;
     int mask_kind, mask_dtype;
@@ -159,18 +161,19 @@ __device__ __forceinline__ float mask_term(const TcParams& p, int b, int h, int 
 // cexp = scale*log2e); with a user mask it is scaled and masked first
 // (cexp = 1).  Masked entries are -inf either way.
 
-template <typename T, bool kMasked>
-__device__ __forceinline__ void mask_tile(float (&s)[128], const TcParams& prm, int b, int h, int row,
+template <typename T, bool kMasked, int NC = 128>
+__device__ __forceinline__ void mask_tile(float (&s)[NC], const TcParams& prm, int b, int h, int row,
                                           bool row_ok, int kv0) {
+    static_assert(NC % 4 == 0, "whole 32-bit mask words");
     if constexpr (kMasked) {
-        const int n = row_ok ? min(128, prm.Skv - kv0) : 0;  // keys of this row inside the tile
+        const int n = row_ok ? min(NC, prm.Skv - kv0) : 0;  // keys of this row inside the tile
         const unsigned char* mrow = static_cast<const unsigned char*>(prm.mask) + b * prm.sm0 + h * prm.sm1 +
                                     (long long)row * prm.sm2 + kv0;
         if (prm.mask_kind == kMaskBool && n > 0 && (reinterpret_cast<uintptr_t>(mrow) & 3) == 0) {
             // bool mask: four keys per 32-bit load (the per-key byte loads of a
             // row-per-thread layout would each cost a separate memory request)
 #pragma unroll
-            for (int w = 0; w < 32; ++w) {
+            for (int w = 0; w < NC / 4; ++w) {
                 uint32_t m4 = 0;
                 if (4 * w + 4 <= n) {
                     m4 = *reinterpret_cast<const uint32_t*>(mrow + 4 * w);
@@ -185,7 +188,7 @@ __device__ __forceinline__ void mask_tile(float (&s)[128], const TcParams& prm, 
             }
         } else {
 #pragma unroll
-            for (int x = 0; x < 128; ++x) {
+            for (int x = 0; x < NC; ++x) {
                 const float add = x < n ? mask_term<T>(prm, b, h, row, kv0 + x) : -CUDART_INF_F;
                 s[x] = fmaf(s[x], prm.c2, add);
             }
@@ -194,9 +197,9 @@ __device__ __forceinline__ void mask_tile(float (&s)[128], const TcParams& prm, 
     int lim = prm.Skv - 1 - kv0;  // last visible key offset in this tile
     if (prm.causal) lim = min(lim, row - kv0);
     if (!row_ok) lim = -1;
-    if (lim < 127) {
+    if (lim < NC - 1) {
 #pragma unroll
-        for (int x = 0; x < 128; ++x) s[x] = (x > lim) ? -CUDART_INF_F : s[x];
+        for (int x = 0; x < NC; ++x) s[x] = (x > lim) ? -CUDART_INF_F : s[x];
     }
 }
 
@@ -1079,6 +1082,517 @@ tc_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         tc_fence_after();
         if (*abort_flag) {
             // give in-flight TMA / tcgen05 work time to land before freeing TMEM
+            for (int i = 0; i < 200; ++i) __nanosleep(1000);
+        }
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------- one-sweep cluster kernel
+// The whole forward in one Q K^T sweep.  The live key tiles of a 128-row
+// query block are dealt round-robin over a cluster of C CTAs (tile j to CTA
+// j % C, at most kMaxOwn tiles each), and every CTA keeps the exponentials of
+// its tiles in TMEM instead of recomputing the scores:
+//   A  S_j = Q K_j^T (tcgen05, TMEM); per row and per 64-key half tile the max
+//      m_j, e = exp2(s - m_j) rounded to fp16 and kept in TMEM, and the row's
+//      running (max, sum of exp2);
+//   B  every CTA sends its rows' (max, sum) into each cluster CTA's shared
+//      memory (st.async, completing on that CTA's mbarrier): every CTA then
+//      holds the exact row LSE of the whole key range;
+//   C  P = e * exp2(m_j - lse) in the output dtype, written back over e in TMEM
+//      (the A operand of O_part += P V_j) and, per warp, into a 128B-swizzled
+//      32 x 64 shared box that a TMA store copies to P;
+//   D  every CTA sends the partial-O rows CTA c owns ([ceil(128 c / C),
+//      ceil(128 (c + 1) / C))) from registers into c's shared memory
+//      (st.async); c adds them to its own partial rows and stores O.
+// P is normalised by the final LSE, as in the two-sweep form; the one extra
+// rounding is that of e to fp16 (relative 2^-12 on values in (0, 1], so at
+// most ~2.5e-4 absolute on P), inside the half-ulp of an f16 / bf16 P.
+// K and V are read once per query block, Q K^T runs once and exp2 runs once
+// per score.  Clusters are persistent over query blocks (heaviest causal
+// blocks first, snake order over clusters).  All cross-CTA traffic is
+// st.async into the receiver's shared memory, completing on the receiver's
+// own mbarriers; the statistics of block k reach a CTA only after it has
+// finished block k - 1, which orders every reuse of its receive slots.
+//
+// Shared memory: a ring of K / V tile slots, the Q tile (refilled for the
+// next block once the last Q K^T has read it), one 32 x 64 P box per worker
+// warp, the receive area (the peers' partial-O rows, then their statistics
+// in its last C KB), the warpgroup merge area, barriers.  TMEM: S in
+// [0, 128), e / P of own tile i in [128 + 64 i, 192 + 64 i) as packed 16-bit
+// pairs (warpgroup g: 32 columns at + 32 g), O in [384, 384 + D).
+//   warp 0       TMA producer: per block Q, then the CTA's K tiles, then its V tiles
+//   warp 1       TMEM allocator + MMA issuer
+//   warps 2, 3   zero-fill of this CTA's rows of P above the causal diagonal
+//   warps 4..11  two softmax warpgroups; warpgroup g takes keys [64 g, 64 g + 64)
+//                of every tile
+template <int D>
+struct OneCfg {
+    static constexpr int kChunks = D / 64;
+    static constexpr int kTile = 128 * D * 2;      // one 128-row Q / K / V tile
+    static constexpr int kMaxOwn = 4;              // key tiles a CTA keeps per query block
+    static constexpr int kBoxBytes = 32 * 128;     // one warp's 32-row x 64-key P box
+    static constexpr int kRecvBytes = 64 * 1024;   // partial-O rows of the peers + their statistics
+    static constexpr int kMergeBytes = 1024;       // warpgroup 1's (max, sum) per row
+    static constexpr int kBarBytes = 256;
+    static constexpr int kMaxSmem = 227 * 1024;
+    static constexpr int kFixed = kTile + 8 * kBoxBytes + kRecvBytes + kMergeBytes + kBarBytes + 1024;
+    static constexpr int kSlots = (kMaxSmem - kFixed) / kTile > 6 ? 6 : (kMaxSmem - kFixed) / kTile;
+    static constexpr int kOffRing = 0;
+    static constexpr int kOffQ = kOffRing + kSlots * kTile;
+    static constexpr int kOffBox = kOffQ + kTile;
+    static constexpr int kOffRecv = kOffBox + 8 * kBoxBytes;
+    static constexpr int kOffMerge = kOffRecv + kRecvBytes;
+    static constexpr int kOffBar = kOffMerge + kMergeBytes;
+    static constexpr int kSmem = kOffBar + kBarBytes + 1024;  // + alignment slack
+    static constexpr uint32_t kColS = 0, kColE = 128, kColO = 384;
+    static constexpr int bQF = 0;               // Q tile landed (TMA)
+    static constexpr int bQE = 1;               // Q tile read by the block's last Q K^T (MMA commit)
+    static constexpr int bF = 2;                // [kSlots] ring slot full (TMA)
+    static constexpr int bE = bF + kSlots;      // [kSlots] ring slot consumed (MMA commit)
+    static constexpr int bSF = bE + kSlots;     // S full (MMA commit)
+    static constexpr int bSE = bSF + 1;         // S read out (256 worker arrivals)
+    static constexpr int bPF = bSE + 1;         // [kMaxOwn] P of own tile i in TMEM (256 worker arrivals)
+    static constexpr int bO = bPF + kMaxOwn;    // partial O complete (MMA commit)
+    static constexpr int bOE = bO + 1;          // partial O read out of TMEM (one worker arrival)
+    static constexpr int bST = bOE + 1;         // every cluster CTA's statistics landed (1 arrival + bytes)
+    static constexpr int bRecv = bST + 1;       // the peers' partial-O rows landed (1 arrival + bytes)
+    static constexpr int kBars = bRecv + 1;
+    static_assert(kBars * 8 + 16 <= kBarBytes, "barrier block");
+    static_assert(kSlots >= 3, "ring too shallow");
+    // (C - 1) slots of ceil(128 / C) rows (at most 114 rows, C = 7) + C KB of
+    // statistics, for every C <= 8
+    static_assert(114 * D * 4 + 7 * 1024 <= kRecvBytes && 112 * D * 4 + 8 * 1024 <= kRecvBytes, "receive area");
+    static_assert(kSmem <= kMaxSmem, "shared memory budget");
+    static_assert(kColO + D <= 512 && kColE + 64 * kMaxOwn <= kColO, "TMEM budget");
+};
+constexpr int kOneMaxCluster = 8;  // portable cluster size: up to 32 live key tiles per query block
+
+struct OneItem {
+    int b, h, qt, n;  // batch, head, query tile, live key tiles
+};
+
+// Query blocks in decreasing causal weight: rank r -> query tile
+// n_qtiles - 1 - r / (B * Hq), then (b, h).
+__device__ __forceinline__ OneItem one_item(const TcParams& prm, int r) {
+    const int bh = prm.B * prm.Hq;
+    OneItem I;
+    I.qt = prm.n_qtiles - 1 - r / bh;
+    const int x = r % bh;
+    I.b = x / prm.Hq;
+    I.h = x % prm.Hq;
+    I.n = live_tiles(prm, I.qt);
+    return I;
+}
+
+// The k-th query block of cluster c among G clusters (snake order).
+__device__ __forceinline__ int one_rank(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
+
+// Bounded wait whose phase may be completed from a peer CTA (acquire at
+// cluster scope).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                 uint32_t role, uint32_t idx) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait_cluster(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort_flag = 1;
+            atomicCAS(&g_status_word, 0u, (role << 24) | ((idx & 0xffu) << 16) | (blockIdx.x & 0xffffu));
+            return false;
+        }
+    }
+    return true;
+}
+
+template <int D, typename T, bool kMasked>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_onesweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_p,
+                   const TcParams prm) {
+    using C = OneCfg<D>;
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sRing = smem_u32(smem + C::kOffRing);
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sBox = smem_u32(smem + C::kOffBox);
+    const uint32_t sRecv = smem_u32(smem + C::kOffRecv);
+    float* mgM = reinterpret_cast<float*>(smem + C::kOffMerge);
+    float* mgL = mgM + 128;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    auto bar = [&](int i) { return smem_u32(bars + i); };
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int CL = prm.cl;
+    const uint32_t rank = cluster_ctarank();
+    const int cl = (int)blockIdx.x / CL, G = (int)gridDim.x / CL;
+    const int n_items = prm.B * prm.Hq * prm.n_qtiles;
+    // key tiles of query block I this CTA owns: rank, rank + C, ...
+    auto n_own_of = [&](const OneItem& I) { return I.n > (int)rank ? (I.n - (int)rank + CL - 1) / CL : 0; };
+    // first O row of the slice CTA c reduces (row t belongs to CTA t * C / 128)
+    auto row_begin = [&](int c) { return (c * 128 + CL - 1) / CL; };
+    // the peers' statistics, float2 [C][128], in the last C KB of the receive area
+    const uint32_t sStat = sRecv + C::kRecvBytes - CL * 1024;
+
+    // ------------------------------------------------------------ set-up
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < C::kBars; ++i) mbar_init(bar(i), 1);
+        mbar_init(bar(C::bSE), 256);
+        for (int i = 0; i < C::kMaxOwn; ++i) mbar_init(bar(C::bPF + i), 256);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    cluster_barrier();  // barriers initialised in every CTA before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < 4) {
+        setmaxnreg_dec<kRegsLow>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            int it = 0, q_use = 0;
+            auto load_tile = [&](uint32_t dst, const CUtensorMap* tm, uint32_t full, uint32_t ord, int row0, int head,
+                                 int b) {
+                mbar_arrive_expect_tx(full, C::kTile);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(dst + c * 16384, tm, full, c * 64, pick(ord & 3, row0, head, b),
+                                pick((ord >> 2) & 3, row0, head, b), pick((ord >> 4) & 3, row0, head, b));
+            };
+            auto load = [&](const CUtensorMap* tm, uint32_t ord, int row0, int head, int b) {
+                const int s = it % C::kSlots;
+                wait_bar(bar(C::bE + s), ((it / C::kSlots) & 1) ^ 1, abort_flag, 1, C::bE + s);
+                load_tile(sRing + s * C::kTile, tm, bar(C::bF + s), ord, row0, head, b);
+                ++it;
+            };
+            for (int k = 0;; ++k) {
+                const int r = one_rank(k, cl, G);
+                if (r >= n_items) break;
+                const OneItem I = one_item(prm, r);
+                const int no = n_own_of(I), hk = I.h / prm.group;
+                if (no == 0) continue;
+                wait_bar(bar(C::bQE), (q_use & 1) ^ 1, abort_flag, 1, C::bQE);
+                load_tile(sQ, &tm_q, bar(C::bQF), prm.ord_q, I.qt * 128, I.h, I.b);
+                ++q_use;
+                for (int i = 0; i < no; ++i) load(&tm_k, prm.ord_k, ((int)rank + CL * i) * 128, hk, I.b);
+                for (int i = 0; i < no; ++i) load(&tm_v, prm.ord_v, ((int)rank + CL * i) * 128, hk, I.b);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
+            constexpr uint32_t idesc_pv = idesc_f16(128, D, kBF16, true);
+            const uint64_t rdesc0 = sw128_desc(sRing, 16, 1024);     // K: K-major
+            const uint64_t qd = sw128_desc(sQ, 16, 1024);            // Q: K-major
+            const uint64_t vdesc0 = sw128_desc(sRing, 16384, 1024);  // V: N-major, 64-column chunks 16 KB apart
+            int it = 0, s_use = 0, q_use = 0;
+            uint32_t pf_phase = 0;
+            for (int k = 0;; ++k) {
+                const int r = one_rank(k, cl, G);
+                if (r >= n_items) break;
+                const OneItem I = one_item(prm, r);
+                const int no = n_own_of(I);
+                if (no > 0) {
+                    wait_bar(bar(C::bQF), q_use & 1, abort_flag, 2, C::bQF);
+                    ++q_use;
+                    for (int i = 0; i < no; ++i) {
+                        const int s = it % C::kSlots;
+                        wait_bar(bar(C::bF + s), (it / C::kSlots) & 1, abort_flag, 2, C::bF + s);
+                        wait_bar(bar(C::bSE), (s_use & 1) ^ 1, abort_flag, 2, C::bSE);
+                        tc_fence_after();
+                        const uint64_t kd = rdesc0 + static_cast<uint64_t>((s * C::kTile) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint64_t off = static_cast<uint64_t>(((kk / 4) * 16384 + (kk % 4) * 32) >> 4);
+                            tc_mma_f16(tmem + C::kColS, qd + off, kd + off, idesc_qk, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(bar(C::bSF));
+                        tc_commit(bar(C::bE + s));
+                        ++it;
+                        ++s_use;
+                    }
+                    tc_commit(bar(C::bQE));  // the Q tile, once the last Q K^T has read it
+                }
+                // the previous block's O has left TMEM before this block's P V (or,
+                // with no tile here, its completion signal): bO never runs two
+                // phases ahead of the workers
+                if (k > 0) wait_bar(bar(C::bOE), (k - 1) & 1, abort_flag, 2, C::bOE);
+                for (int i = 0; i < no; ++i) {
+                    const int s = it % C::kSlots;
+                    wait_bar(bar(C::bF + s), (it / C::kSlots) & 1, abort_flag, 2, C::bF + s);
+                    wait_bar(bar(C::bPF + i), (pf_phase >> i) & 1, abort_flag, 2, C::bPF + i);
+                    pf_phase ^= 1u << i;
+                    tc_fence_after();
+                    const uint64_t vd = vdesc0 + static_cast<uint64_t>((s * C::kTile) >> 4);
+                    // O += P_i V_i: P from TMEM (keys 16 kk .. 16 kk + 15 in columns 8 kk ..)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        tc_mma_f16_ts(tmem + C::kColO, tmem + C::kColE + 64 * i + 8 * kk,
+                                      vd + static_cast<uint64_t>((kk * 2048) >> 4), idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(bar(C::bE + s));
+                    ++it;
+                }
+                // every block, also one without tiles here: the workers wait for it
+                tc_commit(bar(C::bO));
+            }
+        } else if (warp >= 2) {
+            // ------------------------------------------------------------ causal zero tiles
+            const int rb = row_begin((int)rank), re = row_begin((int)rank + 1);
+            for (int k = 0;; ++k) {
+                const int r = one_rank(k, cl, G);
+                if (r >= n_items) break;
+                const OneItem I = one_item(prm, r);
+                const int r0 = I.qt * 128;
+                zero_p_region(prm, I.b, I.h, r0 + rb, min(r0 + re, prm.Sq), I.n * 128, warp - 2, 2, lane);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax workers
+        setmaxnreg_inc<kRegsHigh>();
+        const int g = (warp - 4) >> 2;                      // warpgroup: keys [64 g, 64 g + 64) of a tile
+        const int t = (threadIdx.x - 128) & 127;            // row within the block == TMEM lane
+        const int wt = threadIdx.x - 128;                   // 0..255
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const float cexp = kMasked ? 1.f : prm.c2;
+        const int rb = row_begin((int)rank), re = row_begin((int)rank + 1);
+        const int rows_max = (128 + CL - 1) / CL;
+        const int owner = t * CL / 128;                     // CTA that reduces and stores row t of O
+        const int own_slot_row = t - row_begin(owner);
+        constexpr int kRowBytes = D * 4;
+        const uint32_t box = sBox + (warp - 4) * C::kBoxBytes;
+        int s_use = 0;
+        if (lane == 0) prefetch_tmap(&tm_p);
+        for (int k = 0;; ++k) {
+            const int r = one_rank(k, cl, G);
+            if (r >= n_items) break;
+            const OneItem I = one_item(prm, r);
+            const int no = n_own_of(I);
+            const int r0 = I.qt * 128, row = r0 + t;
+            const bool row_ok = row < prm.Sq;
+            // bytes this block will receive (the peers cannot send them before this
+            // CTA has finished the previous block: they need its statistics first)
+            if (wt == 0) {
+                mbar_arrive_expect_tx(bar(C::bST), (uint32_t)(CL * 128 * 8));
+                mbar_arrive_expect_tx(bar(C::bRecv), (uint32_t)((CL - 1) * (re - rb) * kRowBytes));
+            }
+
+            // ---- A: S -> exponentials (fp16, TMEM) and the row's running (max, sum)
+            float M = -CUDART_INF_F, L = 0.f;
+            float mt[C::kMaxOwn];
+#pragma unroll
+            for (int i = 0; i < C::kMaxOwn; ++i) {
+                mt[i] = -CUDART_INF_F;
+                if (i < no) {
+                    const int kv0 = ((int)rank + CL * i) * 128 + 64 * g;
+                    wait_bar(bar(C::bSF), s_use & 1, abort_flag, 4, C::bSF);
+                    tc_fence_after();
+                    float s[64];
+                    tmem_ld64(tmem + lane_base + C::kColS + 64 * g, s);
+                    tc_fence_before();
+                    mbar_arrive(bar(C::bSE));
+                    ++s_use;
+                    mask_tile<T, kMasked, 64>(s, prm, I.b, I.h, row, row_ok, kv0);
+                    float mx[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) mx[x] = s[x];
+#pragma unroll
+                    for (int x = 8; x < 64; ++x) mx[x & 7] = fmaxf(mx[x & 7], s[x]);
+                    const float m_t = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                            fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * cexp;
+                    const float mm = m_t == -CUDART_INF_F ? 0.f : m_t;  // all masked: every e is 0
+                    uint32_t hp[32];
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int x = 0; x < 32; ++x) {
+                        const float e0 = ex2(fmaf(s[2 * x], cexp, -mm));
+                        const float e1 = ex2(fmaf(s[2 * x + 1], cexp, -mm));
+                        acc[x & 3] += e0 + e1;
+                        __half2 hh = __floats2half2_rn(e0, e1);
+                        hp[x] = *reinterpret_cast<uint32_t*>(&hh);
+                    }
+                    tmem_st32(tmem + lane_base + C::kColE + 64 * i + 32 * g, hp);
+                    if (m_t != -CUDART_INF_F) {
+                        const float l_t = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                        const float Mn = fmaxf(M, m_t);
+                        L = L * ex2(M - Mn) + l_t * ex2(m_t - Mn);
+                        M = Mn;
+                    }
+                    mt[i] = m_t;
+                }
+            }
+
+            // ---- B: the row LSE over the whole cluster.  The warpgroups merge
+            // their (max, sum) here; warpgroup 0 sends the CTA's pair of every
+            // row into every cluster CTA's statistics slots.
+            if (g == 1) {
+                mgM[t] = M;
+                mgL[t] = L;
+            }
+            softmax_group_sync();
+            if (g == 0) {
+                const float M1 = mgM[t], L1 = mgL[t];
+                const float Mc = fmaxf(M, M1);
+                const float Lc = Mc == -CUDART_INF_F ? 0.f : L * ex2(M - Mc) + L1 * ex2(M1 - Mc);
+                const uint32_t slot = sStat + (rank * 128 + t) * 8;
+                for (int c = 0; c < CL; ++c)
+                    st_async_v2(cluster_addr(slot, c), Mc, Lc, cluster_addr(bar(C::bST), c));
+            }
+            wait_bar_cluster(bar(C::bST), k & 1, abort_flag, 5, C::bST);
+            float lse2;
+            {
+                const float2* st = reinterpret_cast<const float2*>(smem + C::kOffRecv + C::kRecvBytes - CL * 1024);
+                float2 sv[kOneMaxCluster];
+                float Mx = -CUDART_INF_F;
+#pragma unroll
+                for (int c = 0; c < kOneMaxCluster; ++c) {
+                    sv[c] = make_float2(-CUDART_INF_F, 0.f);
+                    if (c < CL) {
+                        sv[c] = st[c * 128 + t];
+                        Mx = fmaxf(Mx, sv[c].x);
+                    }
+                }
+                if (Mx == -CUDART_INF_F) {
+                    lse2 = -CUDART_INF_F;
+                } else {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kOneMaxCluster; ++c)
+                        if (c < CL) sum += sv[c].y * ex2(sv[c].x - Mx);
+                    lse2 = Mx + log2f(sum);
+                }
+            }
+            const bool dead = lse2 == -CUDART_INF_F;
+
+            // ---- C: P = e * exp2(m_j - lse): back into TMEM for P V, and through the
+            // warp's swizzled box to a TMA store of P
+#pragma unroll
+            for (int i = 0; i < C::kMaxOwn; ++i) {
+                if (i < no) {
+                    const int kv0 = ((int)rank + CL * i) * 128 + 64 * g;
+                    const float sc = (dead || mt[i] == -CUDART_INF_F) ? 0.f : ex2(mt[i] - lse2);
+                    const uint32_t ecol = tmem + lane_base + C::kColE + 64 * i + 32 * g;
+                    float ef[32];
+                    tmem_ld32(ecol, ef);
+                    uint32_t w[32];
+                    if constexpr (kBF16) {
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const uint32_t bits = __float_as_uint(ef[x]);
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&bits));
+                            w[x] = Pack<T>::two(f.x * sc, f.y * sc);
+                        }
+                    } else {
+                        // f16: one packed multiply per pair (e, the factor and the
+                        // product each rounded to f16: at most 3 * 2^-12 relative)
+                        const __half2 sc2 = __float2half2_rn(sc);
+#pragma unroll
+                        for (int x = 0; x < 32; ++x) {
+                            const uint32_t bits = __float_as_uint(ef[x]);
+                            __half2 hh = __hmul2(*reinterpret_cast<const __half2*>(&bits), sc2);
+                            w[x] = *reinterpret_cast<uint32_t*>(&hh);
+                        }
+                    }
+                    tmem_st32(ecol, w);
+                    tc_fence_before();
+                    mbar_arrive(bar(C::bPF + i));
+                    // the box is free once this warp's previous P store has read it
+                    if (lane == 0) bulk_wait_read0();
+                    __syncwarp();
+                    const uint32_t rowaddr = box + (t & 31) * 128;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        st_shared_v4(rowaddr + ((u ^ (t & 7)) * 16), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int prow = r0 + 32 * (warp & 3);
+                        tma_store_4d(&tm_p, box, kv0, pick(prm.ord_p & 3, prow, I.h, I.b),
+                                     pick((prm.ord_p >> 2) & 3, prow, I.h, I.b),
+                                     pick((prm.ord_p >> 4) & 3, prow, I.h, I.b));
+                        bulk_commit();
+                    }
+                }
+            }
+
+            // ---- D: partial O rows to their owners (st.async, 16-byte units of row
+            // t at unit ^ (t % 8)); this CTA adds the peers' rows to its own
+            wait_bar(bar(C::bO), k & 1, abort_flag, 6, C::bO);
+            tc_fence_after();
+            float ov[D / 2];
+            if (no > 0) {
+                if constexpr (D == 128) tmem_ld64(tmem + lane_base + C::kColO + g * 64, ov);
+                else tmem_ld32(tmem + lane_base + C::kColO + g * 32, ov);
+            } else {
+#pragma unroll
+                for (int x = 0; x < D / 2; ++x) ov[x] = 0.f;
+            }
+            tc_fence_before();
+            softmax_group_sync();  // O is out of TMEM
+            if (wt == 0) mbar_arrive(bar(C::bOE));
+            if (owner != (int)rank) {
+                const int slot = (int)rank < owner ? (int)rank : (int)rank - 1;
+                const uint32_t dst = cluster_addr(sRecv + (slot * rows_max + own_slot_row) * kRowBytes, owner);
+                const uint32_t rbar = cluster_addr(bar(C::bRecv), owner);
+#pragma unroll
+                for (int u = 0; u < D / 8; ++u) {
+                    const int pu = (g * (D / 8) + u) ^ (t & 7);
+                    st_async_v4(dst + pu * 16, __float_as_uint(ov[4 * u]), __float_as_uint(ov[4 * u + 1]),
+                                __float_as_uint(ov[4 * u + 2]), __float_as_uint(ov[4 * u + 3]), rbar);
+                }
+            }
+            wait_bar_cluster(bar(C::bRecv), k & 1, abort_flag, 6, C::bRecv);
+            if (owner == (int)rank) {
+#pragma unroll
+                for (int sl = 0; sl < kOneMaxCluster - 1; ++sl) {
+                    if (sl < CL - 1) {
+                        const uint32_t src = sRecv + (sl * rows_max + own_slot_row) * kRowBytes;
+#pragma unroll
+                        for (int u = 0; u < D / 8; ++u) {
+                            const int pu = (g * (D / 8) + u) ^ (t & 7);
+                            const uint4 a = ld_shared_v4(src + pu * 16);
+                            ov[4 * u] += __uint_as_float(a.x);
+                            ov[4 * u + 1] += __uint_as_float(a.y);
+                            ov[4 * u + 2] += __uint_as_float(a.z);
+                            ov[4 * u + 3] += __uint_as_float(a.w);
+                        }
+                    }
+                }
+                if (row_ok) {
+                    T* op = static_cast<T*>(prm.o) + I.b * prm.so0 + I.h * prm.so1 + (long long)row * prm.so2 + g * (D / 2);
+#pragma unroll
+                    for (int u = 0; u < D / 16; ++u) {
+                        uint4 w4;
+                        w4.x = Pack<T>::two(ov[8 * u], ov[8 * u + 1]);
+                        w4.y = Pack<T>::two(ov[8 * u + 2], ov[8 * u + 3]);
+                        w4.z = Pack<T>::two(ov[8 * u + 4], ov[8 * u + 5]);
+                        w4.w = Pack<T>::two(ov[8 * u + 6], ov[8 * u + 7]);
+                        reinterpret_cast<uint4*>(op)[u] = w4;
+                    }
+                }
+            }
+            if (rank == 0 && g == 0 && prm.lse && row_ok)
+                prm.lse[((long long)I.b * prm.Hq + I.h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
+            softmax_group_sync();  // the receive area is read before this CTA's statistics of the next block go out
+        }
+        if (lane == 0) bulk_wait0();
+    }
+
+    // ------------------------------------------------------------ teardown
+    tc_fence_before();
+    __syncthreads();
+    cluster_barrier();  // no CTA leaves while a peer may still write into its shared memory
+    if (warp == 1) {
+        tc_fence_after();
+        if (*abort_flag) {
             for (int i = 0; i < 200; ++i) __nanosleep(1000);
         }
         tmem_dealloc(tmem, 512);
@@ -2474,6 +2988,116 @@ cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Clusters of `cl` CTAs of the one-sweep kernel that can be resident at once
+// on this device (0 when none can be placed), cached per (kernel, size).
+struct ClusterFit {
+    const void* kern;
+    int dev, cl, n;
+};
+std::mutex g_fit_mu;
+ClusterFit g_fit[32];
+int g_fit_n = 0;
+
+template <typename K>
+int resident_clusters(K kern, int cl, int smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const void* key = reinterpret_cast<const void*>(kern);
+    std::lock_guard<std::mutex> lock(g_fit_mu);
+    for (int i = 0; i < g_fit_n; ++i)
+        if (g_fit[i].kern == key && g_fit[i].dev == dev && g_fit[i].cl == cl) return g_fit[i].n;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)cl, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 0;
+    }
+    if (g_fit_n < 32) g_fit[g_fit_n++] = ClusterFit{key, dev, cl, n};
+    return n;
+}
+
+// CTAs per cluster of the one-sweep kernel: enough that no CTA keeps more
+// than kMaxOwn key tiles of a query block (0: the rows are too long).
+int onesweep_cluster(const Problem& p) {
+    const int64_t n = max_live_key_tiles(p.Sq, p.Skv, p.causal != 0);
+    const int64_t cl = (n + 3) / 4;
+    return cl >= 1 && cl <= kOneMaxCluster ? (int)cl : 0;
+}
+
+template <int D, typename T, bool kMasked>
+cudaError_t launch_onesweep(const Problem& p, cudaStream_t stream) {
+    using C = OneCfg<D>;
+    static_assert(C::kMaxOwn == 4, "onesweep_cluster assumes four tiles per CTA");
+    const int cl = onesweep_cluster(p);
+    if (cl == 0) return cudaErrorNotSupported;
+    CUtensorMap mq, mk, mv, mp, mo;
+    TcParams prm;
+    std::memset(&prm, 0, sizeof(prm));
+    // (the O map only validates the layout: O rows are stored with 16-byte stores)
+    if (!make_map(&mq, p.dtype, p.q, p.D, p.Sq, p.Hq, p.B, p.sq, 128, &prm.ord_q) ||
+        !make_map(&mk, p.dtype, p.k, p.D, p.Skv, p.Hkv, p.B, p.sk, 128, &prm.ord_k) ||
+        !make_map(&mv, p.dtype, p.v, p.Dv, p.Skv, p.Hkv, p.B, p.sv, 128, &prm.ord_v) ||
+        !make_map(&mp, p.dtype, p.p, p.Skv, p.Sq, p.Hq, p.B, p.sp, 32, &prm.ord_p) ||
+        !make_map(&mo, p.dtype, p.o, p.Dv, p.Sq, p.Hq, p.B, p.so, 32, &prm.ord_o))
+        return cudaErrorNotSupported;
+    prm.Sq = (int)p.Sq;
+    prm.Skv = (int)p.Skv;
+    prm.Hq = (int)p.Hq;
+    prm.group = (int)p.group;
+    prm.n_qtiles = (int)((p.Sq + 127) / 128);
+    prm.causal = p.causal;
+    prm.B = (int)p.B;
+    prm.cl = cl;
+    prm.c2 = p.scale * kLog2e;
+    prm.mask = p.mask;
+    prm.mask_kind = p.mask_kind;
+    prm.mask_dtype = p.mask_dtype;
+    prm.sm0 = p.sm[0]; prm.sm1 = p.sm[1]; prm.sm2 = p.sm[2];
+    prm.o = p.o;
+    prm.so0 = p.so[0]; prm.so1 = p.so[1]; prm.so2 = p.so[2];
+    prm.lse = p.lse;
+    prm.p = p.p;
+    prm.sp0 = p.sp[0]; prm.sp1 = p.sp[1]; prm.sp2 = p.sp[2];
+    auto kern = tc_onesweep_kernel<D, T, kMasked>;
+    cudaError_t e = prepare_kernel(kern, C::kSmem);
+    if (e != cudaSuccess) return e;
+    const int fit = resident_clusters(kern, cl, C::kSmem);
+    if (fit <= 0) return cudaErrorNotSupported;
+    const long long items = p.B * p.Hq * (long long)prm.n_qtiles;
+    if (items > (1ll << 30)) return cudaErrorNotSupported;
+    int G = (int)(items < fit ? items : fit);
+    // test / profiling hook: fewer clusters, so each walks more query blocks
+    const char* cap_env = std::getenv("SDPA_MATH_ONESWEEP_CLUSTERS");
+    const int cap = cap_env ? std::atoi(cap_env) : 0;
+    if (cap > 0 && cap < G) G = cap;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(G * cl), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)C::kSmem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mp, prm);
+    return e;
+}
+
 int sm_count() {
     static int n = [] {
         int dev = 0, v = 0;
@@ -2514,6 +3138,11 @@ cudaError_t launch_qt(const Problem& p, cudaStream_t stream) {
 
 template <typename T>
 cudaError_t launch_t(const Problem& p, int mode, cudaStream_t stream) {
+    if (mode == 4) {
+        const bool masked = p.mask_kind != kMaskNone;
+        if (p.D == 64) return masked ? launch_onesweep<64, T, true>(p, stream) : launch_onesweep<64, T, false>(p, stream);
+        return masked ? launch_onesweep<128, T, true>(p, stream) : launch_onesweep<128, T, false>(p, stream);
+    }
     if (mode == 3) {
         const bool masked = p.mask_kind != kMaskNone;
         if (p.D == 64) return masked ? launch_fused<64, T, true>(p, stream) : launch_fused<64, T, false>(p, stream);
@@ -2785,9 +3414,19 @@ cudaError_t launch_bwd_tc(const BwdProblem& p, cudaStream_t stream) {
     return p.D == 64 ? launch_bwd_tc_t<64, __nv_bfloat16>(p, stream) : launch_bwd_tc_t<128, __nv_bfloat16>(p, stream);
 }
 
+bool onesweep_supports(const Problem& p, const char** why) {
+    if (!tc_supports(p, false, why)) return false;
+    if (onesweep_cluster(p) == 0) {
+        *why = "the one-sweep kernel keeps at most 32 live 128-key tiles per row block (8 CTAs x 4)";
+        return false;
+    }
+    return true;
+}
+
 cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream) {
     const char* why;
-    if (mode < 1 || mode > 3 || !tc_supports(p, mode == 3, &why)) return cudaErrorNotSupported;
+    if (mode < 1 || mode > 4) return cudaErrorNotSupported;
+    if (mode == 4 ? !onesweep_supports(p, &why) : !tc_supports(p, mode == 3, &why)) return cudaErrorNotSupported;
     return p.dtype == kF16 ? launch_t<__half>(p, mode, stream) : launch_t<__nv_bfloat16>(p, mode, stream);
 }
 

@@ -69,7 +69,7 @@ def _full_check(q, k, v, mask, causal, scale, variant="auto", check_lse=True):
 def _variants_for(q, k, v, mask, causal):
     """Every kernel family that accepts this call (the SIMT one always does)."""
     out = []
-    for name in ("simt", "twopass", "paired", "fused", "decode", "split", "tcdecode"):
+    for name in ("simt", "twopass", "paired", "fused", "onesweep", "decode", "split", "tcdecode"):
         try:
             sm.sdpa_math_plan(q, k, v, mask, is_causal=causal, variant=name)
             out.append(name)
@@ -172,6 +172,31 @@ def test_small_cases_every_variant(idx):
     assert "simt" in variants
     for variant in variants:
         _full_check(q, k, v, m, causal, scale, variant)
+
+
+# The one-sweep kernel's clusters are persistent over query blocks.  With the
+# grid capped to two clusters every cluster walks many blocks, causal blocks
+# whose short rows leave some cluster ranks without a key tile (those ranks
+# still take part in the statistics exchange and the O reduction), and blocks
+# of every cluster size up to 4 CTAs.
+ONESWEEP_PERSISTENT = [
+    (1, 3, 3, 640, 640, 64, "f16", True, None),       # 2 CTAs per cluster
+    (1, 2, 1, 1040, 1040, 128, "bf16", True, None),   # 3
+    (2, 2, 2, 520, 648, 64, "f16", False, "bool"),    # 2, every rank busy
+    (1, 4, 2, 1000, 1000, 128, "f16", True, None),    # 2, GQA
+    (1, 2, 2, 1600, 1600, 64, "f16", True, None),     # 4
+]
+
+
+@pytest.mark.parametrize("idx", range(len(ONESWEEP_PERSISTENT)),
+                         ids=lambda i: "x".join(str(x) for x in ONESWEEP_PERSISTENT[i]))
+@pytest.mark.parametrize("clusters", [1, 2])
+def test_onesweep_persistent_clusters(idx, clusters, monkeypatch):
+    B, Hq, Hkv, Sq, Skv, D, dt, causal, mask = ONESWEEP_PERSISTENT[idx]
+    monkeypatch.setenv("SDPA_MATH_ONESWEEP_CLUSTERS", str(clusters))
+    q, k, v, m = W.make_custom(300 + idx, B, Hq, Hkv, Sq, Skv, D, dt, mask=mask)
+    scale = 1.0 / math.sqrt(D)
+    _full_check(q, k, v, m, causal, scale, "onesweep")
 
 
 # --------------------------------------------------------------------------- edge cases
