@@ -72,6 +72,11 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Cluster barrier that publishes nothing (a CTA's shared memory stays alive
+// until every peer is done with it): no wait for this thread's global stores.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+}
 // Address of the same shared-memory word in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t peer_addr(const void* p, uint32_t rank) {
     uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(p)), remote;
@@ -286,15 +291,14 @@ decode_kernel(const DecParams p) {
     }
     __syncthreads();
 
-    // ---- 4. P for the chunk (stored, then kept rounded for P V)
+    // ---- 4. P for the chunk, rounded to the dtype and kept for P V (stored to
+    // global memory after the next cluster barrier, whose release then has
+    // no global stores of this thread to wait for)
     for (int e = t; e < R * n; e += kThreads) {
         const int r = e / n, j = e % n;
         const float L = lse_s[r];
         const float pr = (L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L);
-        const T pt = from_f<T>(pr);
-        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
-        prow[k0 + j] = pt;
-        ss[r * p.chunk + j] = to_f(pt);
+        ss[r * p.chunk + j] = to_f(from_f<T>(pr));
     }
     cp_async_wait_all();
     __syncthreads();
@@ -315,8 +319,13 @@ decode_kernel(const DecParams p) {
         *reinterpret_cast<float2*>(&op[r * Dv + d]) = make_float2(a0, a1);
     }
 
-    // ---- 5. sum this CTA's slice of the O columns over the cluster
+    // ---- 5. sum this CTA's slice of the O columns over the cluster; store P
     cluster_sync();
+    for (int e = t; e < R * n; e += kThreads) {
+        const int r = e / n, j = e % n;
+        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
+        prow[k0 + j] = from_f<T>(ss[r * p.chunk + j]);
+    }
     const int cols = (Dv + C - 1) / C;
     const int c0 = (int)crank * cols, c1 = min(Dv, c0 + cols);
     for (int e = t; e < R * max(0, c1 - c0); e += kThreads) {
@@ -337,7 +346,7 @@ decode_kernel(const DecParams p) {
         const float L = lse_s[t];
         p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
     }
-    cluster_sync();  // no CTA leaves while a peer may still read its shared memory
+    cluster_sync_relaxed();  // no CTA leaves while a peer may still read its shared memory
 }
 
 

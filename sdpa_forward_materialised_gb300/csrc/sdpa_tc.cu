@@ -1681,7 +1681,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-    const int warp = threadIdx.x / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = blockIdx.x, b = blockIdx.y, qt = blockIdx.z;
     const int hk = h / prm.group;
     const int r0 = qt * 128;
@@ -1713,44 +1713,17 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
         load_tile_sw128<T>(sK + j * L::kTile, K, io.sk2, nv, D);
         load_tile_sw128<T>(sV + j * L::kTile, V, io.sv2, nv, D);
     }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    // S_j = Q K_j^T for both key tiles, one commit
-    if (threadIdx.x == 0) {
-        constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
-        for (int j = 0; j < n_kv; ++j)
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-                tc_mma_f16(tmem + j * 128, sw128_desc(sQ + off, 16, 1024),
-                           sw128_desc(sK + j * L::kTile + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-            }
-        tc_commit(smem_u32(&bars[0]));
-    }
-
-    const int wg = threadIdx.x / 128, t = threadIdx.x % 128;
-    const int row = r0 + t;
-    const bool row_ok = row < prm.Sq;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const bool mine = wg < n_kv;  // this warpgroup owns key tile wg
-    const float cexp = kMasked ? 1.f : prm.c2;
-    float s[128];
+    asm volatile("cp.async.commit_group;" ::: "memory");
     // A bool mask is read once per CTA with coalesced loads (warp w takes rows
     // w, w+8, ...; lanes take consecutive 4-byte words, or bytes when the rows
-    // are not 4-byte aligned) and staged in shared memory; the loads are issued
-    // before S is ready, the stores after (the staging area may alias K).
+    // are not 4-byte aligned) while the tiles are in flight, and staged in
+    // shared memory once S is ready (the staging area may alias K).
     constexpr int kMaskRowsPerWarp = 16;
     uint32_t mreg[kMaskRowsPerWarp][2];
     const bool stage_mask = kMasked && prm.mask_kind == kMaskBool;
     const unsigned char* mbase = static_cast<const unsigned char*>(prm.mask) + b * prm.sm0 + h * prm.sm1;
     const bool m_words = stage_mask && ((reinterpret_cast<uintptr_t>(mbase) | (uintptr_t)prm.sm2) & 3) == 0;
     if (stage_mask) {
-        const int lane = threadIdx.x % 32;
 #pragma unroll
         for (int i = 0; i < kMaskRowsPerWarp; ++i) {
             const int rr = warp + 8 * i, grow = r0 + rr;
@@ -1775,11 +1748,36 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
             }
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // S_j = Q K_j^T for both key tiles, one commit
+    if (threadIdx.x == 0) {
+        constexpr uint32_t idesc_qk = idesc_f16(128, 128, kBF16, false);
+        for (int j = 0; j < n_kv; ++j)
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+                tc_mma_f16(tmem + j * 128, sw128_desc(sQ + off, 16, 1024),
+                           sw128_desc(sK + j * L::kTile + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+            }
+        tc_commit(smem_u32(&bars[0]));
+    }
+
+    // warpgroup g takes keys [64 g, 64 g + 64) of every live tile, row t
+    const int wg = threadIdx.x / 128, t = threadIdx.x % 128;
+    const int row = r0 + t;
+    const bool row_ok = row < prm.Sq;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float cexp = kMasked ? 1.f : prm.c2;
     wait_bar(smem_u32(&bars[0]), 0, abort_flag, 7, 0);
     tc_fence_after();
     const uint32_t sMask = smem_u32(smem + L::kOffMask);
     if (stage_mask) {
-        const int lane = threadIdx.x % 32;
 #pragma unroll
         for (int i = 0; i < kMaskRowsPerWarp; ++i) {
             const int rr = warp + 8 * i;
@@ -1800,37 +1798,44 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
         }
         __syncthreads();
     }
+    float s[FusedCfg::kMaxKeyTiles][64];
     float mt = -CUDART_INF_F;
-    if (mine) {
-        tmem_ld128(tmem + lane_base + wg * 128, s);
-        if (stage_mask) {
-            // keys of this row from the staged tile (zero bytes past Skv / Sq)
-            const uint32_t mrow = sMask + t * L::kMaskPitch + wg * 128;
 #pragma unroll
-            for (int w = 0; w < 32; ++w) {
-                uint32_t m4;
-                asm volatile("ld.shared.b32 %0, [%1];" : "=r"(m4) : "r"(mrow + 4 * w));
+    for (int j = 0; j < FusedCfg::kMaxKeyTiles; ++j) {
+        if (j < n_kv) {
+            const int kv0 = j * 128 + 64 * wg;
+            tmem_ld64(tmem + lane_base + j * 128 + 64 * wg, s[j]);
+            if (stage_mask) {
+                // keys of this row from the staged tile (zero bytes past Skv / Sq)
+                const uint32_t mrow = sMask + t * L::kMaskPitch + kv0;
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    s[4 * w + e] = ((m4 >> (8 * e)) & 0xffu) ? fmaf(s[4 * w + e], prm.c2, 0.f) : -CUDART_INF_F;
+                for (int w = 0; w < 16; ++w) {
+                    uint32_t m4;
+                    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(m4) : "r"(mrow + 4 * w));
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        s[j][4 * w + e] = ((m4 >> (8 * e)) & 0xffu) ? fmaf(s[j][4 * w + e], prm.c2, 0.f) : -CUDART_INF_F;
+                }
+                mask_tile<T, false, 64>(s[j], prm, b, h, row, row_ok, kv0);  // ragged keys / rows
+            } else {
+                mask_tile<T, kMasked, 64>(s[j], prm, b, h, row, row_ok, kv0);
             }
-            mask_tile<T, false>(s, prm, b, h, row, row_ok, wg * 128);  // ragged keys / rows
-        } else {
-            mask_tile<T, kMasked>(s, prm, b, h, row, row_ok, wg * 128);
-        }
-        float mx = s[0];
 #pragma unroll
-        for (int x = 1; x < 128; ++x) mx = fmaxf(mx, s[x]);
-        mt = mx * cexp;
+            for (int x = 0; x < 64; ++x) mt = fmaxf(mt, s[j][x]);
+        }
     }
-    stat[wg * 128 + t] = mt;
+    stat[wg * 128 + t] = mt * cexp;
     __syncthreads();
     const float m = fmaxf(stat[t], stat[128 + t]);
     float lpart = 0.f;
-    if (mine && m != -CUDART_INF_F) {
+    if (m != -CUDART_INF_F) {
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int x = 0; x < 128; ++x) acc[x & 7] += ex2(fmaf(s[x], cexp, -m));
+        for (int j = 0; j < FusedCfg::kMaxKeyTiles; ++j)
+            if (j < n_kv) {
+#pragma unroll
+                for (int x = 0; x < 64; ++x) acc[x & 7] += ex2(fmaf(s[j][x], cexp, -m));
+            }
         lpart = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     }
     stat[256 + wg * 128 + t] = lpart;
@@ -1838,10 +1843,20 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     const float l = stat[256 + t] + stat[384 + t];
     const float lse2 = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
     const bool dead = lse2 == -CUDART_INF_F;
-    uint32_t hp[64];
-    if (mine) {
-        tile_probs<T>(s, cexp, dead ? -CUDART_INF_F : -lse2, hp);
-        store_p_row(hp, sP + wg * 128 * 128 * 2, t);
+    const float neg = dead ? -CUDART_INF_F : -lse2;
+#pragma unroll
+    for (int j = 0; j < FusedCfg::kMaxKeyTiles; ++j) {
+        if (j < n_kv) {
+            uint32_t hp[32];
+#pragma unroll
+            for (int x = 0; x < 32; ++x)
+                hp[x] = Pack<T>::two(ex2(fmaf(s[j][2 * x], cexp, neg)), ex2(fmaf(s[j][2 * x + 1], cexp, neg)));
+            // chunk wg of P tile j, row t (16-byte unit u at u ^ (t % 8))
+            const uint32_t rowaddr = sP + j * 128 * 128 * 2 + wg * 16384 + t * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(rowaddr + ((u ^ (t & 7)) * 16), hp[4 * u], hp[4 * u + 1], hp[4 * u + 2], hp[4 * u + 3]);
+        }
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -1859,32 +1874,35 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
             }
         tc_commit(smem_u32(&bars[1]));
     }
-    // P rows to global memory while P V runs: warp w copies rows w, w+8, ...
-    // out of the swizzled tiles; lanes take consecutive key pairs (4-byte
-    // stores) or, when the caller's P rows are only 2-byte aligned, keys
+    // P rows to global memory while P V runs
     {
-        const int lane = threadIdx.x % 32;
         const int nrows = min(128, prm.Sq - r0);
-        for (int rr = warp; rr < nrows; rr += 8) {
-            uint16_t* prow = static_cast<uint16_t*>(prm.p) + b * prm.sp0 + h * prm.sp1 + (long long)(r0 + rr) * prm.sp2;
-            auto src = [&](int key) {  // shared address of P[rr, key]
-                const int kt = key & 127;
-                return sP + (key >> 7) * (128 * 128 * 2) + (kt >> 6) * 16384 + rr * 128 +
-                       ((((kt >> 3) & 7) ^ (rr & 7)) << 4) + (kt & 7) * 2;
-            };
-            // (live_end is a multiple of 128 or Skv, so a key pair never straddles it)
-            if ((reinterpret_cast<uintptr_t>(prow) & 3) == 0) {
-                for (int key = 2 * lane; key < prm.Skv; key += 64) {
-                    uint32_t v = 0;
-                    if (key < live_end) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src(key)));
-                    if (key + 1 < prm.Skv) *reinterpret_cast<uint32_t*>(prow + key) = v;
-                    else prow[key] = static_cast<uint16_t>(v);
-                }
-            } else {
-                for (int key = lane; key < prm.Skv; key += 32) {
-                    uint16_t v = 0;
-                    if (key < live_end) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(src(key)));
-                    prow[key] = v;
+        // shared address of P[rr, key] (key < live_end)
+        auto src = [&](int rr, int key) {
+            const int kt = key & 127;
+            return sP + (key >> 7) * (128 * 128 * 2) + (kt >> 6) * 16384 + rr * 128 +
+                   ((((kt >> 3) & 7) ^ (rr & 7)) << 4) + (kt & 7) * 2;
+        };
+        uint16_t* pslab = static_cast<uint16_t*>(prm.p) + b * prm.sp0 + h * prm.sp1 + (long long)r0 * prm.sp2;
+        {
+            // row by row: warp w copies rows w, w+8, ...; lanes take consecutive
+            // key pairs (4-byte stores) or, with only 2-byte aligned rows, keys
+            for (int rr = warp; rr < nrows; rr += 8) {
+                uint16_t* prow = pslab + (long long)rr * prm.sp2;
+                // (live_end is a multiple of 128 or Skv, so a key pair never straddles it)
+                if ((reinterpret_cast<uintptr_t>(prow) & 3) == 0) {
+                    for (int key = 2 * lane; key < prm.Skv; key += 64) {
+                        uint32_t v = 0;
+                        if (key < live_end) asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(src(rr, key)));
+                        if (key + 1 < prm.Skv) *reinterpret_cast<uint32_t*>(prow + key) = v;
+                        else prow[key] = static_cast<uint16_t>(v);
+                    }
+                } else {
+                    for (int key = lane; key < prm.Skv; key += 32) {
+                        uint16_t v = 0;
+                        if (key < live_end) asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(src(rr, key)));
+                        prow[key] = v;
+                    }
                 }
             }
         }
