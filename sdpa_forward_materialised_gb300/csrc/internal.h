@@ -81,6 +81,8 @@ cudaError_t launch_tc(const Problem& p, int mode, cudaStream_t stream);
 bool onesweep_supports(const Problem& p, const char** why);
 // Query tiles per CTA that suit the two-pass kernel for p (1 or 2).
 int tc_query_tiles(const Problem& p);
+// Whether AUTO serves p with the one-sweep cluster kernel.
+bool onesweep_auto(const Problem& p);
 bool decode_supports(const Problem& p, const char** why);
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 bool split_supports(const Problem& p, const char** why);

@@ -216,20 +216,24 @@ constexpr int64_t kFusedMaxLiveTiles = 2;
 
 // Variant the AUTO rule picks for a validated problem.  The tensor-core
 // families are ordered by measurement on GB300 (a sweep over live-tile counts
-// 1..16 per row block and 4..8704 tiles per call): the two-pass kernels were
+// 1..16 per row block and 4..16384 tiles per call): the two-pass kernels were
 // faster than the fused one at every shape both could run, so the fused
 // kernel serves the calls whose rows TMA cannot describe (P rows that are not
 // 16-byte multiples) when each row block keeps at most two live key tiles;
-// between the two two-pass layouts the paired grid is taken once it still
-// fills about three quarters of the SMs (tc_query_tiles).
+// the one-sweep cluster kernel takes causal calls whose clusters all fit in
+// one wave (onesweep_auto); between the two two-pass layouts the paired grid
+// is taken once it still fills about three quarters of the SMs
+// (tc_query_tiles).
 sdpa_variant choose(const sdpa::Problem& p) {
     const char* why = nullptr;
     if (p.dtype == SDPA_F32) return SDPA_VARIANT_SIMT;
     if (sdpa::decode_supports(p, &why)) return SDPA_VARIANT_DECODE;
     if (sdpa::tc_decode_supports(p, &why)) return SDPA_VARIANT_TC_DECODE;
     if (sdpa::split_supports(p, &why)) return SDPA_VARIANT_SPLIT;
-    if (sdpa::tc_supports(p, false, &why))
+    if (sdpa::tc_supports(p, false, &why)) {
+        if (sdpa::onesweep_auto(p) && sdpa::onesweep_supports(p, &why)) return SDPA_VARIANT_TC_ONESWEEP;
         return sdpa::tc_query_tiles(p) == 2 ? SDPA_VARIANT_TC_PAIRED : SDPA_VARIANT_TC_TWOPASS;
+    }
     if (sdpa::max_live_key_tiles(p.Sq, p.Skv, p.causal != 0) <= kFusedMaxLiveTiles && sdpa::tc_supports(p, true, &why))
         return SDPA_VARIANT_TC_FUSED;
     return SDPA_VARIANT_SIMT;

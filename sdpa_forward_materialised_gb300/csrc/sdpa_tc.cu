@@ -3130,14 +3130,34 @@ int sm_count() {
 }  // namespace
 
 // Query tiles per CTA: two tiles share every K / V load (half the load traffic
-// per score tile) when that still gives about one CTA per SM and there is no
-// causal mask (with one, a paired CTA's two workers hold unequal tile counts
-// and the one-tile layout, whose workers alternate, measured faster).
+// per score tile) when that still gives about three quarters of a CTA per SM.
+// Measured on GB300 (96 shapes, D 64 / 128): the paired layout wins from about
+// 0.75 pairs per SM, with or without a causal mask, except where a paired
+// CTA's two unequal causal streams cost more than the shared loads save:
+// causal calls past two pairs per SM (1-2 % slower at 512 pairs) and causal
+// D = 128 rows of more than 8 key tiles (2k: 47.1 against 45.8 us).
 int tc_query_tiles(const Problem& p) {
     const int64_t nq = (p.Sq + 127) / 128;
-    if (nq < 2 || p.causal) return 1;
+    if (nq < 2) return 1;
     const int64_t pairs = p.B * p.Hq * ((nq + 1) / 2);
-    return pairs * 4 >= (int64_t)sm_count() * 3 ? 2 : 1;
+    const int64_t sms = sm_count();
+    if (pairs * 4 < sms * 3) return 1;
+    if (p.causal && (pairs > 2 * sms || (p.D > 64 && nq > 8))) return 1;
+    return 2;
+}
+
+// Whether AUTO takes the one-sweep cluster kernel: causal calls whose row
+// blocks need clusters of two or more CTAs and whose clusters all fit in one
+// wave (row blocks x cluster size <= SMs).  There its shorter per-block
+// critical path wins (1x8x8 1024x1024 causal: 16.1 against 20.5 us at D = 64,
+// 18.1 against 22.1 us at D = 128); everywhere else on the same sweep it lost.
+bool onesweep_auto(const Problem& p) {
+    if (!p.causal) return false;
+    const int64_t n = max_live_key_tiles(p.Sq, p.Skv, true);
+    const int64_t cl = (n + 3) / 4;
+    if (cl < 2 || cl > 8) return false;
+    const int64_t blocks = p.B * p.Hq * ((p.Sq + 127) / 128);
+    return blocks * cl <= (int64_t)sm_count();
 }
 
 namespace {

@@ -198,11 +198,12 @@ def test_f32_always_plans_simt(lib):
 
 
 # AUTO's kernel family per benchmark workload (host-only planning): the fused
-# single-sweep kernel for at most two live key tiles per row block, the cluster decode kernel for few rows
+# single-sweep kernel for P rows TMA cannot describe, the cluster decode kernel for few rows
 # per KV head, the tensor-core split-KV kernel when those rows meet a long key
 # sequence at D = 128 (the CUDA-core split-KV kernel at other head dims),
-# the one-tile two-pass kernel under a causal mask, the paired layout for the
-# non-causal GQA prefill, and the CUDA-core kernel for fp32.
+# the one-tile two-pass kernel for the causal prefills (1k D64: 64 query-tile
+# pairs; 2k D128: causal rows of 16 key tiles), the paired layout for the GQA
+# prefill, and the CUDA-core kernel for fp32.
 @pytest.mark.parametrize("name,expect", [
     ("tiny_f32", "simt"), ("prefill1k_d64_f16", "twopass"), ("prefill2k_d128_f16", "twopass"),
     ("prefill2k_d128_bf16", "twopass"), ("gqa1k_d128_f16", "paired"), ("decode_skv1152_f16", "decode"),
@@ -217,6 +218,29 @@ def test_auto_choice_per_workload(lib, name, expect):
     if w.mask is not None:
         m = torch.empty(w.B, 1, w.Sq, w.Skv, dtype=torch.bool)
     assert sm.sdpa_math_plan(q, k, v, m, is_causal=w.is_causal)["variant"] == expect
+
+
+# The tensor-core layout AUTO takes, pinned to the GB300 sweep (96 shapes,
+# f16, L2 flushed, CUDA events) it was calibrated on; each case names the
+# measured times (us) of the layouts involved.
+@pytest.mark.parametrize("B,H,S,D,causal,expect", [
+    (1, 8, 1024, 64, True, "onesweep"),    # onesweep 16.1, twopass 20.5: 64 blocks x 2 CTAs fit one wave
+    (1, 8, 1024, 128, True, "onesweep"),   # onesweep 18.1, twopass 22.1
+    (1, 16, 1024, 64, True, "twopass"),    # twopass 20.1, onesweep 22.2 (256 CTAs), paired 24.3 (64 pairs)
+    (1, 8, 2048, 128, True, "twopass"),    # twopass 36.5, paired 42.6, onesweep 48.8
+    (1, 16, 512, 64, True, "twopass"),     # twopass 16.0, paired 22.1 (one CTA per cluster: no onesweep)
+    (1, 32, 1024, 64, True, "paired"),     # paired 26.2, twopass 30.3 (128 pairs)
+    (1, 32, 1024, 128, True, "paired"),    # paired 30.3, twopass 32.4
+    (1, 16, 2048, 64, True, "paired"),     # paired 39.2, twopass 41.3
+    (1, 16, 2048, 128, True, "twopass"),   # twopass 45.8, paired 47.1 (100-step bench)
+    (1, 64, 512, 128, True, "paired"),     # paired 24.2, twopass 24.9
+    (1, 64, 2048, 64, True, "twopass"),    # twopass 134.8, paired 136.8 (512 pairs)
+    (1, 64, 512, 64, False, "paired"),     # paired 20.1, twopass 26.2
+    (1, 8, 1024, 64, False, "twopass"),    # twopass 20.1, paired 28.3 (no causal mask: no onesweep)
+])
+def test_auto_tensor_core_layout_follows_the_sweep(lib, B, H, S, D, causal, expect):
+    q, k, v = _qkv(B=B, Hq=H, Hkv=H, Sq=S, Skv=S, D=D)
+    assert sm.sdpa_math_plan(q, k, v, is_causal=causal)["variant"] == expect
 
 
 def test_fused_takes_at_most_two_live_key_tiles_per_row_block(lib):
