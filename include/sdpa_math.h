@@ -96,7 +96,7 @@ typedef enum {
     SDPA_VARIANT_TC_ONESWEEP = 8 /* tcgen05, one Q K^T sweep: the live key tiles of a 128-row block
                                     split over a cluster of up to 8 CTAs (4 tiles each, so at most
                                     32 tiles = 4096 keys per row block), exp2(S - tile max) kept in
-                                    shared memory, row LSE by DSMEM, then P = that * exp2(max - lse) */
+                                    TMEM, row LSE by DSMEM, then P = that * exp2(max - lse) */
 } sdpa_variant;
 
 typedef struct {
