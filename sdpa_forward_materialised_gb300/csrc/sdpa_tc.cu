@@ -755,6 +755,7 @@ tc_twopass_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
 
     // ------------------------------------------------------------ teardown
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -1076,6 +1077,7 @@ tc_wide_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     }
 
     // ------------------------------------------------------------ teardown
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -1587,6 +1589,7 @@ tc_onesweep_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 
     // ------------------------------------------------------------ teardown
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     cluster_barrier();  // no CTA leaves while a peer may still write into its shared memory
@@ -1932,6 +1935,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     if (wg == 0 && prm.lse && row_ok)
         prm.lse[((long long)b * prm.Hq + h) * prm.Sq + row] = dead ? lse2 : lse2 * kLn2;
 
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -2220,6 +2224,7 @@ tc_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant
         const float L = lse_s[t];
         p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
     }
+    __syncwarp();  // each warp reaches the cluster-wide barrier converged: lane-0 roles end later than their warp
     cluster_barrier();  // no CTA leaves while a peer may still read its shared memory
     tc_fence_before();
     __syncthreads();
@@ -2507,6 +2512,7 @@ bwd_tc_rows_kernel(const __grid_constant__ CUtensorMap tm_go, const __grid_const
             }
         }
     }
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -2743,6 +2749,7 @@ bwd_tc_keys_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_consta
             }
         }
     }
+    __syncwarp();  // each warp reaches the CTA-wide barrier converged: lane-0 roles end later than their warp
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
