@@ -27,14 +27,22 @@
 // A CTA needs little shared memory (the V chunk, the scores, the partial O),
 // so all clusters of a decode-sized call are resident at once and every K and
 // V read of the call is issued in the first few microseconds.
+//
+// 16-bit calls with head dims of 32, 64, 128 or 256 take stream_decode_kernel
+// instead (same split; K and V stream through a shared-memory ring, both
+// products on the warp-level tensor-core instructions, one cluster exchange);
+// SDPA_MATH_DECODE_KERNEL=cluster keeps them on decode_kernel.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace sdpa {
 namespace {
@@ -107,9 +115,18 @@ struct DecParams {
     int Hq, Sq, Skv, D, Dv, group, rows, chunk, causal;
     float c2;  // scale * log2(e)
     int off_v, off_q, off_s, off_o, off_stat;  // shared-memory layout (bytes)
+    // streaming kernel only
+    int slots, slot_bytes, off_ring, off_pt, off_fac, off_part;
+    int k_contig, v_contig;  // key / value rows back to back (row stride == head dim)
 };
 
 __device__ __forceinline__ void cp_async_wait_ring() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+// All but the newest slots - 1 committed groups of this thread are complete.
+__device__ __forceinline__ void cp_async_wait_pieces(int slots) {
+    if (slots >= 4) asm volatile("cp.async.wait_group 3;" ::: "memory");
+    else if (slots == 3) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 // RM is a compile-time bound on the query rows (R <= RM), so the per-row
 // accumulators of the score phase stay in registers.
@@ -341,6 +358,387 @@ decode_kernel(const DecParams p) {
         const bool dead = lse_s[r] == -CUDART_INF_F;
         T* orow = static_cast<T*>(p.o) + b * p.so0 + row_h[r] * p.so1 + (long long)row_i[r] * p.so2;
         orow[d] = from_f<T>(dead ? 0.f : acc);
+    }
+    if (crank == 0 && p.lse && t < R) {
+        const float L = lse_s[t];
+        p.lse[((long long)b * p.Hq + row_h[t]) * p.Sq + row_i[t]] = (L == -CUDART_INF_F) ? L : L * kLn2;
+    }
+    cluster_sync_relaxed();  // no CTA leaves while a peer may still read its shared memory
+}
+
+
+
+// ---------------------------------------------------------------------------
+// Streaming decode kernel (16-bit inputs; head dims of 32, 64, 128 or 256).
+//
+// The cluster split of decode_kernel (one cluster per (batch, key/value head),
+// CTA rank c owns a contiguous chunk of keys), with another data path inside
+// the CTA:
+//   * K and V stream through a ring of 32-key pieces.  Every thread issues
+//     16-byte asynchronous copies (consecutive threads on consecutive bytes of
+//     a row) and places each 16-byte unit of a row at unit u ^ f(row), an XOR
+//     swizzle that makes the 8-row matrix loads below conflict-free.  A slot
+//     is refilled as soon as the CTA has used it, so each CTA keeps a few
+//     pieces in flight from its first instructions on;
+//   * both products run on the tensor cores with the warp-level
+//     mma.sync.m16n8k16 (fp16 / bf16 operands, fp32 accumulation): the scores
+//     as S^T = K_piece Q^T (16 keys by 8 query rows per instruction), the
+//     output as O += P~ V (the query rows padded to 16, 8 value columns per
+//     instruction);
+//   * the chunk's softmax runs online: one warp per row and one lane per key
+//     keep the running (max, sum); P~ = exp2(s - running max), rounded to the
+//     input dtype, is the A operand of P V, and O is rescaled whenever the
+//     max grows.  The scores stay in shared memory for P;
+//   * one cluster barrier publishes every CTA's (max, sum) and partial O.
+//     Each CTA then forms the same lse, writes its P = exp2(s - lse) and sums
+//     its slice of the O columns over the cluster, the partial of CTA c
+//     weighted by exp2(max_c - lse).
+// ---------------------------------------------------------------------------
+constexpr int kStreamTK = 32;   // keys per piece (one per lane in the row statistics)
+constexpr int kStreamMaxSlots = 4;
+// four CTAs per SM: 228 KB of shared memory per SM, 1 KB reserved per CTA,
+// and a little static shared memory
+constexpr int kStreamSmemTarget = 56 * 1024 - 512;
+constexpr int kPthPitch = kStreamTK + 8;  // P~ tile row pitch (elements): conflict-free fragment loads
+
+// Physical 16-byte unit of logical unit u in row `row` of a tile whose rows
+// hold `units` units (4, 8, 16 or 32): eight consecutive rows read at the same
+// logical unit land in eight different 16-byte bank groups.
+__device__ __forceinline__ int swz(int row, int u, int units) {
+    return units >= 8 ? (u ^ (row & 7)) : (u ^ ((row >> 1) & 3));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+
+// c (16 x 8, fp32) += a (16 x 16, row) * b (16 x 8, col) in the operand dtype T.
+template <typename T> __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1);
+template <> __device__ __forceinline__ void mma16816<__half>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Every thread: start its share of the copies of piece `piece` of the chunk
+// (K rows into the front of ring slot `slot`, V rows behind them, both
+// swizzled) as 16-byte asynchronous copies and commit them as one group.
+// Rows of the slot past the chunk's end get zeros (copies with no source
+// bytes), so P~ V never multiplies a zero by stale shared memory.
+template <typename T>
+__device__ __forceinline__ void stream_issue(const DecParams& p, const T* K, const T* V, int piece, int n,
+                                             uint8_t* slot, int t) {
+    const int j0 = piece * kStreamTK;
+    const int tk = min(kStreamTK, n - j0);
+    const int uk = p.D * (int)sizeof(T) / 16, uv = p.Dv * (int)sizeof(T) / 16;  // 16-byte units per row
+    const int lk = __ffs(uk) - 1, lv = __ffs(uv) - 1;
+    uint8_t* vdst = slot + kStreamTK * uk * 16;
+    for (int c = t; c < tk * uk; c += kThreads) {
+        const int r = c >> lk, u = c & (uk - 1);
+        cp_async16(slot + 16 * (r * uk + swz(r, u, uk)),
+                   reinterpret_cast<const uint8_t*>(K + (long long)(j0 + r) * p.sk2) + 16 * u);
+    }
+    for (int c = t; c < kStreamTK * uv; c += kThreads) {
+        const int r = c >> lv, u = c & (uv - 1);
+        uint8_t* dst = vdst + 16 * (r * uv + swz(r, u, uv));
+        if (r < tk) {
+            cp_async16(dst, reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * u);
+        } else {
+            const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(d), "l"(V) : "memory");
+        }
+    }
+    cp_async_commit();
+}
+
+template <typename T, int RM>
+__global__ void __launch_bounds__(kThreads, RM <= 4 ? 4 : 2)
+stream_decode_kernel(const DecParams p) {
+    static_assert(sizeof(T) == 2, "16-bit inputs");
+    constexpr int NT = RM > 8 ? 2 : 1;  // 8-row tiles of query rows in the score product
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float m_run[kMaxRows], l_run[kMaxRows], alpha_s[kMaxRows], lse_s[kMaxRows];
+    __shared__ int row_h[kMaxRows], row_i[kMaxRows];
+
+    const int t = threadIdx.x, warp = t / 32, lane = t % 32;
+    const int g = lane >> 2, cc = lane & 3;  // fragment row / column pair of this lane
+    const uint32_t crank = cluster_rank();
+    const int C = (int)gridDim.x;  // the cluster spans the x dimension
+    const int b = blockIdx.z, hk = blockIdx.y;
+    const int k0 = (int)crank * p.chunk;
+    const int n = max(0, min(p.Skv, k0 + p.chunk) - k0);  // keys of this CTA (may be 0)
+    const int R = p.rows, D = p.D, Dv = p.Dv;
+    const int npieces = (n + kStreamTK - 1) / kStreamTK;
+    const int slots = p.slots;
+    const int uk = D * (int)sizeof(T) / 16, uv = Dv * (int)sizeof(T) / 16;
+
+    uint8_t* ring = smem + p.off_ring;                         // [slots][slot_bytes]: K piece, V piece
+    float* ss = reinterpret_cast<float*>(smem + p.off_s);      // [R][chunk] scores (base 2, masked)
+    T* qsh = reinterpret_cast<T*>(smem + p.off_q);             // [8 NT][D] query rows, swizzled units
+    T* pth = reinterpret_cast<T*>(smem + p.off_pt);            // [16][kPthPitch] P~ of a piece
+    float* part = reinterpret_cast<float*>(smem + p.off_part); // [4][RM][32] k-group partial scores
+    float* op = reinterpret_cast<float*>(smem + p.off_ring);   // [R][Dv] partial O (the ring, after the loop)
+    float* st = reinterpret_cast<float*>(smem + p.off_stat);   // [R][2] chunk (max, sum)
+    float* fac = reinterpret_cast<float*>(smem + p.off_fac);   // [R][C] weight of each CTA's partial O
+
+    const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
+    const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
+
+    for (int pc = 0; pc < slots; ++pc) {
+        if (pc < npieces) stream_issue(p, K, V, pc, n, ring + pc * p.slot_bytes, t);
+        else cp_async_commit();
+    }
+    if (t < R) {
+        row_h[t] = hk * p.group + t / p.Sq;
+        row_i[t] = t % p.Sq;
+        m_run[t] = -CUDART_INF_F;
+        l_run[t] = 0.f;
+    }
+    // query rows (zero past R), and a zero P~ tile (rows past R stay zero)
+    for (int e = t; e < 8 * NT * D; e += kThreads) {
+        const int r = e / D, d = e % D;
+        T v = from_f<T>(0.f);
+        if (r < R)
+            v = (static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
+                 (long long)(r % p.Sq) * p.sq2)[d];
+        qsh[r * D + 8 * swz(r, d / 8, uk) + d % 8] = v;
+    }
+    for (int e = t; e < 16 * kPthPitch; e += kThreads) pth[e] = from_f<T>(0.f);
+
+    // the output product: warp w owns value columns [8 ntw w, 8 ntw (w + 1))
+    const int nvt = Dv / 8;                      // 8-column tiles
+    const int ntw = nvt >= 8 ? nvt / 8 : 1;      // tiles per warp: 1, 2 or 4
+    const bool pv_warp = warp < (nvt >= 8 ? 8 : nvt);
+    float oc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) oc[i][e] = 0.f;
+
+    const uint32_t ring_u = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+    const uint32_t qsh_u = static_cast<uint32_t>(__cvta_generic_to_shared(qsh));
+
+    for (int pc = 0; pc < npieces; ++pc) {
+        const int s = pc % slots;
+        // this thread's copies of piece pc have landed (those of the next
+        // slots - 1 pieces may still be in flight); the barrier makes every
+        // thread's copies, and the set-up above, visible
+        cp_async_wait_pieces(slots);
+        __syncthreads();
+        const uint32_t kslot = ring_u + s * p.slot_bytes;
+        const uint32_t vslot = kslot + kStreamTK * uk * 16;
+        const int j0 = pc * kStreamTK, tk = min(kStreamTK, n - j0);
+
+        // S^T = K Q^T on all eight warps: warp w takes key tile w & 1 (16 keys)
+        // and k-group w >> 1 (a quarter of the k-steps, alternating between two
+        // accumulators), so no chain of dependent instructions is longer than
+        // two; the groups' partial sums meet in the statistics phase
+        {
+            const int mt = warp & 1, kg = warp >> 1;
+            const int nks = D / 16, per = (nks + 3) / 4;
+            const int ks0 = min(nks, kg * per), ks1 = min(nks, ks0 + per);
+            float c[2][NT][4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < NT; ++i) c[h][i][0] = c[h][i][1] = c[h][i][2] = c[h][i][3] = 0.f;
+            const int mi = lane >> 3, r8 = lane & 7;
+            const int key = 16 * mt + (mi & 1) * 8 + r8;  // this lane's row address for the K matrices
+            for (int ks2 = ks0; ks2 < ks1; ks2 += 2) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int ks = ks2 + h;
+                    if (ks >= ks1) break;
+                    uint32_t qb[NT][2];
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) {
+                        const int qr = 8 * i + r8;  // lanes 0-15 address units 2 ks, 2 ks + 1
+                        ldsm_x2(qsh_u + 16 * (qr * uk + swz(qr, 2 * ks + (mi & 1), uk)), qb[i][0], qb[i][1]);
+                    }
+                    uint32_t a[4];
+                    ldsm_x4(kslot + 16 * (key * uk + swz(key, 2 * ks + (mi >> 1), uk)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                    for (int i = 0; i < NT; ++i) mma16816<T>(c[h][i], a, qb[i][0], qb[i][1]);
+                }
+            }
+            // c[.][i] = partial S^T[key 16 mt + g (+8)][row 8 i + 2 cc (+1)]
+#pragma unroll
+            for (int i = 0; i < NT; ++i)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = 8 * i + 2 * cc + (e & 1), kk = 16 * mt + g + 8 * (e >> 1);
+                    if (row < R) part[(kg * RM + row) * kStreamTK + kk] = c[0][i][e] + c[1][i][e];
+                }
+        }
+        __syncthreads();
+
+        // masking and the online statistics: one warp per row, one lane per key
+        for (int r = warp; r < R; r += kThreads / 32) {
+            float sv = -CUDART_INF_F;
+            if (lane < tk) {
+                const int key = k0 + j0 + lane;
+                const float* pr = part + r * kStreamTK + lane;
+                sv = __fmul_rn((pr[0] + pr[RM * kStreamTK]) + (pr[2 * RM * kStreamTK] + pr[3 * RM * kStreamTK]), p.c2);
+                if (p.causal && key > row_i[r]) sv = -CUDART_INF_F;
+                if (p.mask_kind != kMaskNone) {
+                    const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + key;
+                    if (p.mask_kind == kMaskBool) {
+                        if (static_cast<const unsigned char*>(p.mask)[off] == 0) sv = -CUDART_INF_F;
+                    } else {
+                        const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                             : to_f(static_cast<const T*>(p.mask)[off]);
+                        sv = __fmaf_rn(m, kLog2e, sv);
+                    }
+                }
+                ss[r * p.chunk + j0 + lane] = sv;
+            }
+            float mp = sv;
+            for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+            const float mo = m_run[r];
+            const float mn = fmaxf(mo, mp);
+            const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // a row with no visible key yet adds zeros
+            const float e = ptx::ex2(sv - ms);  // sv = -inf gives 0
+            float sum = e;
+            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            pth[r * kPthPitch + lane] = from_f<T>(e);
+            if (lane == 0) {
+                const float al = ptx::ex2(mo - ms);
+                alpha_s[r] = al;
+                m_run[r] = mn;
+                l_run[r] = l_run[r] * al + sum;
+            }
+        }
+        __syncthreads();
+
+        // O += P~ V: rows g and g + 8 of each of this warp's column tiles
+        if (pv_warp) {
+            const float a_lo = g < R ? alpha_s[g] : 0.f, a_hi = g + 8 < R ? alpha_s[g + 8] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i < ntw) {
+                    oc[i][0] *= a_lo; oc[i][1] *= a_lo;
+                    oc[i][2] *= a_hi; oc[i][3] *= a_hi;
+                }
+            const int mi = lane >> 3, r8 = lane & 7;
+#pragma unroll
+            for (int ks = 0; ks < kStreamTK / 16; ++ks) {
+                uint32_t a[4];
+                a[0] = *reinterpret_cast<const uint32_t*>(&pth[g * kPthPitch + 16 * ks + 2 * cc]);
+                a[1] = *reinterpret_cast<const uint32_t*>(&pth[(g + 8) * kPthPitch + 16 * ks + 2 * cc]);
+                a[2] = *reinterpret_cast<const uint32_t*>(&pth[g * kPthPitch + 16 * ks + 8 + 2 * cc]);
+                a[3] = *reinterpret_cast<const uint32_t*>(&pth[(g + 8) * kPthPitch + 16 * ks + 8 + 2 * cc]);
+                const int key = 16 * ks + (mi & 1) * 8 + r8;  // this lane's row address for the V matrices
+                if (ntw == 1) {
+                    uint32_t b0, b1;
+                    ldsm_x2_t(vslot + 16 * (key * uv + swz(key, warp, uv)), b0, b1);
+                    mma16816<T>(oc[0], a, b0, b1);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; i += 2)
+                        if (i < ntw) {
+                            uint32_t b0, b1, b2, b3;
+                            const int unit = warp * ntw + i + (mi >> 1);
+                            ldsm_x4_t(vslot + 16 * (key * uv + swz(key, unit, uv)), b0, b1, b2, b3);
+                            mma16816<T>(oc[i], a, b0, b1);
+                            mma16816<T>(oc[i + 1], a, b2, b3);
+                        }
+                }
+            }
+        }
+        __syncthreads();  // the slot and the piece's P~ are free again
+        if (pc + slots < npieces) stream_issue(p, K, V, pc + slots, n, ring + s * p.slot_bytes, t);
+        else cp_async_commit();
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // the chunk's partial O (every element owned by one lane of one warp)
+    if (pv_warp) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (i < ntw) {
+                const int col = 8 * (warp * ntw + i) + 2 * cc;
+                if (g < R) *reinterpret_cast<float2*>(&op[g * Dv + col]) = make_float2(oc[i][0], oc[i][1]);
+                if (g + 8 < R) *reinterpret_cast<float2*>(&op[(g + 8) * Dv + col]) = make_float2(oc[i][2], oc[i][3]);
+            }
+    }
+    if (t < R) {
+        st[2 * t] = m_run[t];
+        st[2 * t + 1] = l_run[t];
+    }
+
+    // ---- every CTA's (max, sum) and partial O are published
+    cluster_sync();
+    if (t < R) {
+        float mc[kMaxCluster], lc[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) {
+                mc[c] = ld_peer(peer_addr(&st[2 * t], (uint32_t)c));
+                lc[c] = ld_peer(peer_addr(&st[2 * t + 1], (uint32_t)c));
+            }
+        float m = -CUDART_INF_F;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) m = fmaxf(m, mc[c]);
+        float l = 0.f;
+        if (m != -CUDART_INF_F) {
+#pragma unroll
+            for (int c = 0; c < kMaxCluster; ++c)
+                if (c < C && mc[c] != -CUDART_INF_F) l += lc[c] * exp2f(mc[c] - m);
+        }
+        const float L = (m == -CUDART_INF_F || !(l > 0.f)) ? -CUDART_INF_F : m + log2f(l);
+        lse_s[t] = L;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) fac[t * C + c] = (L == -CUDART_INF_F || mc[c] == -CUDART_INF_F) ? 0.f : exp2f(mc[c] - L);
+    }
+    __syncthreads();
+
+    // this CTA's slice of the O columns, summed over the cluster
+    const int cols = (Dv + C - 1) / C;
+    const int c0 = (int)crank * cols, c1 = min(Dv, c0 + cols);
+    for (int e = t; e < R * max(0, c1 - c0); e += kThreads) {
+        const int r = e / (c1 - c0), d = c0 + e % (c1 - c0);
+        float part[kMaxCluster];
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) part[c] = ld_peer(peer_addr(&op[r * Dv + d], (uint32_t)c));
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kMaxCluster; ++c)
+            if (c < C) acc = fmaf(fac[r * C + c], part[c], acc);
+        const bool dead = lse_s[r] == -CUDART_INF_F;
+        T* orow = static_cast<T*>(p.o) + b * p.so0 + row_h[r] * p.so1 + (long long)row_i[r] * p.so2;
+        orow[d] = from_f<T>(dead ? 0.f : acc);
+    }
+    // P of the chunk
+    for (int e = t; e < R * n; e += kThreads) {
+        const int r = e / n, j = e % n;
+        const float L = lse_s[r];
+        const float pr = (L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L);
+        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
+        prow[k0 + j] = from_f<T>(pr);
     }
     if (crank == 0 && p.lse && t < R) {
         const float L = lse_s[t];
@@ -711,6 +1109,122 @@ cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Shared-memory layout of stream_decode_kernel (the ring gets as many slots,
+// up to four, as keep the CTA within four per SM); false when even two slots
+// exceed the budget.
+bool plan_stream(const Problem& p, DecParams* dp, int* smem) {
+    int C, chunk, smem_cluster;
+    DecParams tmp;
+    plan(p, &C, &chunk, &tmp, &smem_cluster);
+    const long long R = p.group * p.Sq, es = elem_bytes(p.dtype);
+    const long long NT = R > 8 ? 2 : 1;
+    const long long RM = R <= 4 ? 4 : (R <= 8 ? 8 : 16);  // the kernel's row bound
+    const long long slot = (long long)kStreamTK * (p.D + p.Dv) * es;
+    auto al = [](long long x) { return (x + 15) & ~15ll; };
+    for (int slots = kStreamMaxSlots; slots >= 2; --slots) {
+        long long off = 0;
+        const long long off_ring = off;  // ring; after the loop, the partial O
+        off = al(off + std::max((long long)slots * slot, R * p.Dv * 4));
+        const long long off_s = off; off = al(off + R * chunk * 4);
+        const long long off_q = off; off = al(off + 8 * NT * p.D * es);
+        const long long off_pt = off; off = al(off + 16 * kPthPitch * es);
+        const long long off_part = off; off = al(off + 4 * RM * kStreamTK * 4);
+        const long long off_st = off; off = al(off + R * 2 * 4);
+        const long long off_fac = off; off += R * C * 4;
+        if (off > kStreamSmemTarget && slots > 2) continue;
+        if (off > kSmemBudget) return false;
+        dp->slots = slots;
+        dp->slot_bytes = (int)slot;
+        dp->off_ring = (int)off_ring;
+        dp->off_s = (int)off_s;
+        dp->off_q = (int)off_q;
+        dp->off_pt = (int)off_pt;
+        dp->off_part = (int)off_part;
+        dp->off_stat = (int)off_st;
+        dp->off_fac = (int)off_fac;
+        dp->chunk = chunk;
+        *smem = (int)off;
+        return true;
+    }
+    return false;
+}
+
+bool pow2_head_dim(int64_t d) { return d == 32 || d == 64 || d == 128 || d == 256; }
+
+// Whether stream_decode_kernel serves p (decode_supports(p) holds already).
+bool stream_supports(const Problem& p) {
+    if (p.dtype != kF16 && p.dtype != kBF16) return false;
+    if (!pow2_head_dim(p.D) || !pow2_head_dim(p.Dv)) return false;
+    int smem;
+    DecParams dp;
+    return plan_stream(p, &dp, &smem);
+}
+
+// The register-K cluster kernel stays reachable for 16-bit calls through
+// SDPA_MATH_DECODE_KERNEL=cluster.
+bool stream_disabled() {
+    const char* e = std::getenv("SDPA_MATH_DECODE_KERNEL");
+    return e && std::strcmp(e, "cluster") == 0;
+}
+
+template <typename T, int RM>
+cudaError_t launch_stream_rm(const Problem& pr, cudaStream_t stream) {
+    DecParams p;
+    std::memset(&p, 0, sizeof(p));
+    int smem;
+    if (!plan_stream(pr, &p, &smem)) return cudaErrorNotSupported;
+    const int chunk = p.chunk;
+    fill_params(pr, &p);
+    p.chunk = chunk;
+    p.k_contig = pr.sk[2] == pr.D;
+    p.v_contig = pr.sv[2] == pr.Dv;
+    int C, chunk_cluster, smem_cluster;
+    {
+        DecParams tmp;
+        plan(pr, &C, &chunk_cluster, &tmp, &smem_cluster);  // the cluster size plan_stream laid out for
+    }
+
+    auto kern = stream_decode_kernel<T, RM>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        bool ready = false;
+        for (int i = 0; i < g_nready; ++i)
+            ready |= g_ready[i].kern == reinterpret_cast<const void*>(kern) && g_ready[i].dev == dev;
+        if (!ready) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+            if (e != cudaSuccess) return e;
+            if (g_nready < 32) g_ready[g_nready++] = Ready{reinterpret_cast<const void*>(kern), dev};
+        }
+    }
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)C, (unsigned)pr.Hkv, (unsigned)pr.B);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_stream_t(const Problem& p, cudaStream_t stream) {
+    const int64_t rows = p.group * p.Sq;
+    if (rows <= 4) return launch_stream_rm<T, 4>(p, stream);
+    if (rows <= 8) return launch_stream_rm<T, 8>(p, stream);
+    return launch_stream_rm<T, 16>(p, stream);
+}
+
 // Shared-memory layout of split_kernel for a cluster of C CTAs; false when it
 // exceeds the budget.
 bool plan_split(const Problem& p, int C, int* chunk, DecParams* dp, int* smem) {
@@ -877,6 +1391,8 @@ cudaError_t launch_split(const Problem& p, cudaStream_t stream) {
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {
     const char* why;
     if (!decode_supports(p, &why)) return cudaErrorNotSupported;
+    if (!stream_disabled() && stream_supports(p))
+        return p.dtype == kF16 ? launch_stream_t<__half>(p, stream) : launch_stream_t<__nv_bfloat16>(p, stream);
     switch (p.dtype) {
         case kF32: return launch_t<float>(p, stream);
         case kF16: return launch_t<__half>(p, stream);

@@ -199,6 +199,48 @@ def test_onesweep_persistent_clusters(idx, clusters, monkeypatch):
     _full_check(q, k, v, m, causal, scale, "onesweep")
 
 
+# The decode family has two kernels: 16-bit calls with head dims of 32, 64,
+# 128 or 256 stream K and V through bulk copies; SDPA_MATH_DECODE_KERNEL=cluster
+# forces the register-K kernel, which otherwise serves fp32 and other head
+# dims.  Both run on every shape below.
+DECODE_SHAPES = [
+    # B, Hq, Hkv, Sq, Skv, D, Dv, dtype, causal, mask
+    (2, 8, 2, 1, 1152, 128, 128, "f16", False, None),
+    (1, 4, 2, 1, 300, 32, 32, "f16", False, None),
+    (1, 8, 1, 1, 900, 256, 256, "bf16", False, None),
+    (1, 4, 1, 1, 333, 64, 128, "f16", False, "bool"),       # dead rows, D != Dv
+    (2, 4, 2, 2, 777, 128, 128, "bf16", False, "additive"),
+    (1, 2, 1, 5, 600, 128, 128, "f16", True, None),         # 10 rows; causal rows see 1..5 keys
+    (1, 16, 1, 1, 2048, 64, 64, "f16", False, None),        # 16 rows, 256-key chunks
+    (1, 4, 2, 1, 9, 128, 128, "bf16", False, None),         # fewer keys than one piece
+]
+
+
+@pytest.mark.parametrize("kernel", ["stream", "cluster"])
+@pytest.mark.parametrize("idx", range(len(DECODE_SHAPES)), ids=lambda i: "x".join(str(x) for x in DECODE_SHAPES[i]))
+def test_decode_kernels(idx, kernel, monkeypatch):
+    B, Hq, Hkv, Sq, Skv, D, Dv, dt, causal, mask = DECODE_SHAPES[idx]
+    if kernel == "cluster":
+        monkeypatch.setenv("SDPA_MATH_DECODE_KERNEL", "cluster")
+    else:
+        monkeypatch.delenv("SDPA_MATH_DECODE_KERNEL", raising=False)
+    q, k, v, m = W.make_custom(400 + idx, B, Hq, Hkv, Sq, Skv, D, dt, mask=mask, Dv=Dv)
+    _full_check(q, k, v, m, causal, 1.0 / math.sqrt(D), "decode")
+
+
+def test_decode_rows_not_back_to_back():
+    """K/V stored [B, S, H, D] (row stride H*D): the streaming decode kernel
+    copies them row by row."""
+    q, k, v, _ = W.make_custom(410, 2, 8, 2, 1, 1152, 128, "f16")
+    kt = k.transpose(1, 2).contiguous().transpose(1, 2)
+    vt = v.transpose(1, 2).contiguous().transpose(1, 2)
+    assert kt.stride(2) == 2 * 128
+    O, P, _ = _run(q, kt, vt, None, False, 1.0 / math.sqrt(128), "decode")
+    Or, Pr, _ = oracle_fwd(q, k, v, None, scale=1.0 / math.sqrt(128), nthreads=NTHREADS)
+    compare(O, Or, q.dtype, "O", extra=o_allowance(Pr, v, 4, q.dtype))
+    compare(P, Pr, q.dtype, "P")
+
+
 # --------------------------------------------------------------------------- edge cases
 
 def test_empty_query_is_a_noop():
