@@ -1624,6 +1624,7 @@ struct FusedIO {
     const void* k; long long sk0, sk1, sk2;
     const void* v; long long sv0, sv1, sv2;
     uint32_t tmem_cols;  // power of two >= S columns + D
+    int rpc;             // query rows per CTA: 128, or 32 to spread a small grid over more SMs
 };
 
 struct FusedCfg {
@@ -1687,12 +1688,13 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int h = blockIdx.x, b = blockIdx.y, qt = blockIdx.z;
     const int hk = h / prm.group;
-    const int r0 = qt * 128;
+    const int r0 = qt * io.rpc;
+    const int r_end = min(r0 + io.rpc, prm.Sq);  // this CTA's rows are [r0, r_end)
     // live key tiles of this row block (1 or 2): with a causal mask the keys
     // past its last row are masked for every row, so they are never computed
     // and their P columns are written as zeros
     int n_kv = (prm.Skv + 127) / 128;
-    if (prm.causal) n_kv = min(n_kv, min(min(r0 + 127, prm.Sq - 1), prm.Skv - 1) / 128 + 1);
+    if (prm.causal) n_kv = min(n_kv, min(r_end - 1, prm.Skv - 1) / 128 + 1);
     const int live_end = min(prm.Skv, n_kv * 128);  // keys [live_end, Skv) have P = 0 in every row
     const uint32_t kTmemO = n_kv * 128;             // O columns follow the S tiles
 
@@ -1708,7 +1710,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     }
     // Q tile, K and V tiles -> swizzled operand tiles
     const T* Q = static_cast<const T*>(io.q) + b * io.sq0 + h * io.sq1 + (long long)r0 * io.sq2;
-    load_tile_sw128<T>(sQ, Q, io.sq2, min(128, prm.Sq - r0), D);
+    load_tile_sw128<T>(sQ, Q, io.sq2, r_end - r0, D);
     for (int j = 0; j < n_kv; ++j) {
         const T* K = static_cast<const T*>(io.k) + b * io.sk0 + hk * io.sk1 + (long long)(j * 128) * io.sk2;
         const T* V = static_cast<const T*>(io.v) + b * io.sv0 + hk * io.sv1 + (long long)(j * 128) * io.sv2;
@@ -1733,7 +1735,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
 #pragma unroll
             for (int hw = 0; hw < 2; ++hw) {
                 uint32_t v = 0;
-                if (grow < prm.Sq) {
+                if (grow < r_end) {
                     const unsigned char* mr = mbase + (long long)grow * prm.sm2;
                     if (m_words) {
                         const int k4 = 4 * (lane + 32 * hw);
@@ -1774,7 +1776,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     // warpgroup g takes keys [64 g, 64 g + 64) of every live tile, row t
     const int wg = threadIdx.x / 128, t = threadIdx.x % 128;
     const int row = r0 + t;
-    const bool row_ok = row < prm.Sq;
+    const bool row_ok = row < r_end;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float cexp = kMasked ? 1.f : prm.c2;
     wait_bar(smem_u32(&bars[0]), 0, abort_flag, 7, 0);
@@ -1879,7 +1881,7 @@ tc_fused_kernel(const TcParams prm, const FusedIO io) {
     }
     // P rows to global memory while P V runs
     {
-        const int nrows = min(128, prm.Sq - r0);
+        const int nrows = r_end - r0;
         // shared address of P[rr, key] (key < live_end)
         auto src = [&](int rr, int key) {
             const int kt = key & 127;
@@ -2977,6 +2979,8 @@ cudaError_t launch_wide(const Problem& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+int sm_count();  // SMs of the current device (cached)
+
 template <int D, typename T, bool kMasked>
 cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
     using L = FusedSmem<D>;
@@ -3005,10 +3009,14 @@ cudaError_t launch_fused(const Problem& p, cudaStream_t stream) {
     io.v = p.v; io.sv0 = p.sv[0]; io.sv1 = p.sv[1]; io.sv2 = p.sv[2];
     const uint32_t need = (uint32_t)(max_live_key_tiles(p.Sq, p.Skv, p.causal != 0) * 128 + D);
     io.tmem_cols = need <= 256 ? 256u : 512u;
+    // a grid that leaves most SMs idle takes 32-row query groups instead of
+    // 128-row tiles (four times the CTAs, each a quarter of the rows to
+    // finish and copy out), as long as the finer grid still fits one wave
+    io.rpc = p.B * p.Hq * prm.n_qtiles * 4 <= sm_count() ? 32 : 128;
     auto kern = tc_fused_kernel<D, T, kMasked>;
     cudaError_t e = prepare_kernel(kern, L::kSmem, false);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)prm.n_qtiles);
+    dim3 grid((unsigned)p.Hq, (unsigned)p.B, (unsigned)((p.Sq + io.rpc - 1) / io.rpc));
     kern<<<grid, FusedCfg::kThreads, L::kSmem, stream>>>(prm, io);
     return cudaGetLastError();
 }

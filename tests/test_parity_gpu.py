@@ -138,6 +138,9 @@ SMALL = [
     (1, 2, 2, 100, 100, 64, "bf16", False, "bool"),
     (1, 2, 1, 7, 1, 64, "f16", False, None),
     (1, 3, 3, 250, 129, 128, "bf16", False, "additive"),
+    # the same kernel on a grid large enough to keep 128-row query tiles (small
+    # grids take 32-row query groups): 4 * 16 * 2 tiles
+    (4, 16, 4, 200, 100, 64, "f16", False, "bool"),
     # causal calls whose row blocks keep at most two live key tiles however
     # long the key sequence (the fused kernel writes the masked tail of P as
     # zeros), incl. a P row of odd length
