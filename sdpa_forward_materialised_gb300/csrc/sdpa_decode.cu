@@ -453,16 +453,21 @@ __device__ __forceinline__ void stream_issue(const DecParams& p, const T* K, con
     const int uk = p.D * (int)sizeof(T) / 16, uv = p.Dv * (int)sizeof(T) / 16;  // 16-byte units per row
     const int lk = __ffs(uk) - 1, lv = __ffs(uv) - 1;
     uint8_t* vdst = slot + kStreamTK * uk * 16;
+    // rows back to back (row stride == head dim): the piece is one contiguous
+    // block and unit c of it sits at byte 16 c
+    const uint8_t* kp = reinterpret_cast<const uint8_t*>(K + (long long)j0 * p.sk2);
+    const uint8_t* vp = reinterpret_cast<const uint8_t*>(V + (long long)j0 * p.sv2);
     for (int c = t; c < tk * uk; c += kThreads) {
         const int r = c >> lk, u = c & (uk - 1);
         cp_async16(slot + 16 * (r * uk + swz(r, u, uk)),
-                   reinterpret_cast<const uint8_t*>(K + (long long)(j0 + r) * p.sk2) + 16 * u);
+                   p.k_contig ? kp + 16 * c : reinterpret_cast<const uint8_t*>(K + (long long)(j0 + r) * p.sk2) + 16 * u);
     }
     for (int c = t; c < kStreamTK * uv; c += kThreads) {
         const int r = c >> lv, u = c & (uv - 1);
         uint8_t* dst = vdst + 16 * (r * uv + swz(r, u, uv));
         if (r < tk) {
-            cp_async16(dst, reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * u);
+            cp_async16(dst, p.v_contig ? vp + 16 * c
+                                       : reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * u);
         } else {
             const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(d), "l"(V) : "memory");
@@ -515,8 +520,9 @@ stream_decode_kernel(const DecParams p) {
         l_run[t] = 0.f;
     }
     // query rows (zero past R), and a zero P~ tile (rows past R stay zero)
+    const int ld = __ffs(D) - 1;  // D is a power of two
     for (int e = t; e < 8 * NT * D; e += kThreads) {
-        const int r = e / D, d = e % D;
+        const int r = e >> ld, d = e & (D - 1);
         T v = from_f<T>(0.f);
         if (r < R)
             v = (static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
@@ -733,12 +739,11 @@ stream_decode_kernel(const DecParams p) {
         orow[d] = from_f<T>(dead ? 0.f : acc);
     }
     // P of the chunk
-    for (int e = t; e < R * n; e += kThreads) {
-        const int r = e / n, j = e % n;
+    for (int r = 0; r < R; ++r) {
         const float L = lse_s[r];
-        const float pr = (L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L);
-        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2;
-        prow[k0 + j] = from_f<T>(pr);
+        T* prow = static_cast<T*>(p.p) + b * p.sp0 + row_h[r] * p.sp1 + (long long)row_i[r] * p.sp2 + k0;
+        for (int j = t; j < n; j += kThreads)
+            prow[j] = from_f<T>((L == -CUDART_INF_F) ? 0.f : exp2f(ss[r * p.chunk + j] - L));
     }
     if (crank == 0 && p.lse && t < R) {
         const float L = lse_s[t];
