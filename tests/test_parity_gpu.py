@@ -244,6 +244,49 @@ def test_decode_rows_not_back_to_back():
     compare(P, Pr, q.dtype, "P")
 
 
+# --------------------------------------------------------------------------- seeded random shapes
+
+def _random_cases(n, seed):
+    """Shapes drawn from a fixed seed: dtypes, head dims (80 and D != Dv reach
+    the CUDA-core and register-K kernels only), GQA groups, decode-like rows
+    over long key sequences, ragged lengths, causal calls and both mask kinds."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for _ in range(n):
+        dt = str(rng.choice(["f16", "bf16", "f32"], p=[0.45, 0.45, 0.10]))
+        D = int(rng.choice([32, 64, 80, 128]))
+        Dv = D if rng.random() < 0.85 else int(rng.choice([32, 64, 128]))
+        Hkv, group = int(rng.choice([1, 2, 3])), int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        if rng.random() < 0.35:
+            Sq, Skv = int(rng.integers(1, 5)), int(rng.integers(1, 1500))
+        else:
+            Sq, Skv = int(rng.integers(1, 300)), int(rng.integers(1, 600))
+        causal = bool(rng.random() < 0.3)
+        mask = None if causal or rng.random() < 0.5 else str(rng.choice(["bool", "additive"]))
+        cases.append((B, Hkv * group, Hkv, Sq, Skv, D, Dv, dt, causal, mask))
+    return cases
+
+
+RANDOM = _random_cases(64, 2024)
+
+
+@pytest.mark.parametrize("idx", range(len(RANDOM)), ids=lambda i: "x".join(str(x) for x in RANDOM[i]))
+def test_random_shapes_every_variant(idx):
+    B, Hq, Hkv, Sq, Skv, D, Dv, dt, causal, mask = RANDOM[idx]
+    q, k, v, m = W.make_custom(900 + idx, B, Hq, Hkv, Sq, Skv, D, dt, mask=mask, Dv=Dv)
+    scale = 1.0 / math.sqrt(D)
+    Or, Pr, lr = oracle_fwd(q, k, v, m, is_causal=causal, scale=scale, nthreads=NTHREADS)
+    dead = np.isneginf(lr)
+    for variant in ["auto"] + _variants_for(q, k, v, m, causal):
+        O, P, L = _run(q, k, v, m, causal, scale, variant, lse=True)
+        compare(O, Or, q.dtype, f"O {variant}", extra=o_allowance(Pr, v, Hq // Hkv, q.dtype))
+        compare(P, Pr, q.dtype, f"P {variant}")
+        Lg = L.double().cpu().numpy()
+        assert np.all(np.isneginf(Lg[dead])), f"{variant}: LSE of fully masked rows must be -inf"
+        np.testing.assert_allclose(Lg[~dead], lr[~dead], rtol=2e-6, atol=2e-5)
+
+
 # --------------------------------------------------------------------------- edge cases
 
 def test_empty_query_is_a_noop():
