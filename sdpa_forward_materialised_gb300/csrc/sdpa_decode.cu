@@ -395,11 +395,10 @@ decode_kernel(const DecParams p) {
 //     weighted by exp2(max_c - lse).
 // ---------------------------------------------------------------------------
 constexpr int kStreamTK = 32;   // keys per piece (one per lane in the row statistics)
-constexpr int kStreamMaxSlots = 4;
-// four CTAs per SM: 228 KB of shared memory per SM, 1 KB reserved per CTA,
-// and a little static shared memory
-constexpr int kStreamSmemTarget = 56 * 1024 - 512;
 constexpr int kPthPitch = kStreamTK + 8;  // P~ tile row pitch (elements): conflict-free fragment loads
+constexpr int kKSlots = 2, kVSlots = 4;   // K / V ring slots (32-key pieces)
+constexpr int kGroupThreads = 128;        // each of the two warp groups
+constexpr int kBarGroup = 1, kBarFull = 2, kBarFree = 4;  // named barrier ids: copy group; [2] P~ ready; [2] P~ used
 
 // Physical 16-byte unit of logical unit u in row `row` of a tile whose rows
 // hold `units` units (4, 8, 16 or 32): eight consecutive rows read at the same
@@ -411,9 +410,6 @@ __device__ __forceinline__ int swz(int row, int u, int units) {
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr) : "memory");
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
 }
 __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -440,31 +436,30 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float* c, const uint32_t
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Every thread: start its share of the copies of piece `piece` of the chunk
-// (K rows into the front of ring slot `slot`, V rows behind them, both
-// swizzled) as 16-byte asynchronous copies and commit them as one group.
-// Rows of the slot past the chunk's end get zeros (copies with no source
+// Every thread of the copy group (warps 0-3): start its share of the copies
+// of piece `piece` of the chunk (K rows into K slot `kslot`, V rows into V
+// slot `vslot`, both swizzled) as 16-byte asynchronous copies and commit them
+// as one group.  V rows past the chunk's end get zeros (copies with no source
 // bytes), so P~ V never multiplies a zero by stale shared memory.
 template <typename T>
 __device__ __forceinline__ void stream_issue(const DecParams& p, const T* K, const T* V, int piece, int n,
-                                             uint8_t* slot, int t) {
+                                             uint8_t* kslot, uint8_t* vslot, int ta) {
     const int j0 = piece * kStreamTK;
     const int tk = min(kStreamTK, n - j0);
     const int uk = p.D * (int)sizeof(T) / 16, uv = p.Dv * (int)sizeof(T) / 16;  // 16-byte units per row
     const int lk = __ffs(uk) - 1, lv = __ffs(uv) - 1;
-    uint8_t* vdst = slot + kStreamTK * uk * 16;
     // rows back to back (row stride == head dim): the piece is one contiguous
     // block and unit c of it sits at byte 16 c
     const uint8_t* kp = reinterpret_cast<const uint8_t*>(K + (long long)j0 * p.sk2);
     const uint8_t* vp = reinterpret_cast<const uint8_t*>(V + (long long)j0 * p.sv2);
-    for (int c = t; c < tk * uk; c += kThreads) {
+    for (int c = ta; c < tk * uk; c += kGroupThreads) {
         const int r = c >> lk, u = c & (uk - 1);
-        cp_async16(slot + 16 * (r * uk + swz(r, u, uk)),
+        cp_async16(kslot + 16 * (r * uk + swz(r, u, uk)),
                    p.k_contig ? kp + 16 * c : reinterpret_cast<const uint8_t*>(K + (long long)(j0 + r) * p.sk2) + 16 * u);
     }
-    for (int c = t; c < kStreamTK * uv; c += kThreads) {
+    for (int c = ta; c < kStreamTK * uv; c += kGroupThreads) {
         const int r = c >> lv, u = c & (uv - 1);
-        uint8_t* dst = vdst + 16 * (r * uv + swz(r, u, uv));
+        uint8_t* dst = vslot + 16 * (r * uv + swz(r, u, uv));
         if (r < tk) {
             cp_async16(dst, p.v_contig ? vp + 16 * c
                                        : reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * u);
@@ -476,17 +471,45 @@ __device__ __forceinline__ void stream_issue(const DecParams& p, const T* K, con
     cp_async_commit();
 }
 
+// Named barriers (immediate ids, so the kernel reserves only those it uses):
+// bar.sync waits, bar.arrive only counts; every warp of a group executes them.
+template <int ID, int N> __device__ __forceinline__ void nbar_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+template <int ID, int N> __device__ __forceinline__ void nbar_arrive() {
+    asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(N) : "memory");
+}
+// the two-slot handshakes between the warp groups, by the parity of the piece
+__device__ __forceinline__ void full_arrive(int i) {
+    if (i & 1) nbar_arrive<kBarFull + 1, 2 * kGroupThreads>();
+    else nbar_arrive<kBarFull, 2 * kGroupThreads>();
+}
+__device__ __forceinline__ void full_sync(int i) {
+    if (i & 1) nbar_sync<kBarFull + 1, 2 * kGroupThreads>();
+    else nbar_sync<kBarFull, 2 * kGroupThreads>();
+}
+__device__ __forceinline__ void free_arrive(int i) {
+    if (i & 1) nbar_arrive<kBarFree + 1, 2 * kGroupThreads>();
+    else nbar_arrive<kBarFree, 2 * kGroupThreads>();
+}
+__device__ __forceinline__ void free_sync(int i) {
+    if (i & 1) nbar_sync<kBarFree + 1, 2 * kGroupThreads>();
+    else nbar_sync<kBarFree, 2 * kGroupThreads>();
+}
+
 template <typename T, int RM>
 __global__ void __launch_bounds__(kThreads, RM <= 4 ? 4 : 2)
 stream_decode_kernel(const DecParams p) {
     static_assert(sizeof(T) == 2, "16-bit inputs");
     constexpr int NT = RM > 8 ? 2 : 1;  // 8-row tiles of query rows in the score product
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float m_run[kMaxRows], l_run[kMaxRows], alpha_s[kMaxRows], lse_s[kMaxRows];
+    __shared__ float m_run[kMaxRows], l_run[kMaxRows], alpha_s[2][kMaxRows], lse_s[kMaxRows];
     __shared__ int row_h[kMaxRows], row_i[kMaxRows];
 
     const int t = threadIdx.x, warp = t / 32, lane = t % 32;
     const int g = lane >> 2, cc = lane & 3;  // fragment row / column pair of this lane
+    const int mi = lane >> 3, r8 = lane & 7;  // this lane's matrix / row in an 8x8 matrix load
+    const bool copy_group = warp < 4;
     const uint32_t crank = cluster_rank();
     const int C = (int)gridDim.x;  // the cluster spans the x dimension
     const int b = blockIdx.z, hk = blockIdx.y;
@@ -494,200 +517,205 @@ stream_decode_kernel(const DecParams p) {
     const int n = max(0, min(p.Skv, k0 + p.chunk) - k0);  // keys of this CTA (may be 0)
     const int R = p.rows, D = p.D, Dv = p.Dv;
     const int npieces = (n + kStreamTK - 1) / kStreamTK;
-    const int slots = p.slots;
     const int uk = D * (int)sizeof(T) / 16, uv = Dv * (int)sizeof(T) / 16;
+    const int kbytes = kStreamTK * uk * 16, vbytes = kStreamTK * uv * 16;
 
-    uint8_t* ring = smem + p.off_ring;                         // [slots][slot_bytes]: K piece, V piece
+    uint8_t* kring = smem + p.off_ring;               // [kKSlots][32 rows of K]
+    uint8_t* vring = kring + kKSlots * kbytes;        // [kVSlots][32 rows of V]
     float* ss = reinterpret_cast<float*>(smem + p.off_s);      // [R][chunk] scores (base 2, masked)
-    T* qsh = reinterpret_cast<T*>(smem + p.off_q);             // [8 NT][D] query rows, swizzled units
-    T* pth = reinterpret_cast<T*>(smem + p.off_pt);            // [16][kPthPitch] P~ of a piece
-    float* part = reinterpret_cast<float*>(smem + p.off_part); // [4][RM][32] k-group partial scores
-    float* op = reinterpret_cast<float*>(smem + p.off_ring);   // [R][Dv] partial O (the ring, after the loop)
+    T* pth = reinterpret_cast<T*>(smem + p.off_pt);            // [2][16][kPthPitch] P~ of a piece
+    float* part = reinterpret_cast<float*>(smem + p.off_part); // [2][RM][32] k-group partial scores
+    float* op = reinterpret_cast<float*>(smem + p.off_ring);   // [R][Dv] partial O (the rings, after the loop)
     float* st = reinterpret_cast<float*>(smem + p.off_stat);   // [R][2] chunk (max, sum)
     float* fac = reinterpret_cast<float*>(smem + p.off_fac);   // [R][C] weight of each CTA's partial O
 
     const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
     const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
 
-    for (int pc = 0; pc < slots; ++pc) {
-        if (pc < npieces) stream_issue(p, K, V, pc, n, ring + pc * p.slot_bytes, t);
-        else cp_async_commit();
-    }
+    if (copy_group)
+        for (int pc = 0; pc < 2; ++pc) {
+            if (pc < npieces) stream_issue(p, K, V, pc, n, kring + (pc & 1) * kbytes, vring + (pc & 3) * vbytes, t);
+            else cp_async_commit();
+        }
     if (t < R) {
         row_h[t] = hk * p.group + t / p.Sq;
         row_i[t] = t % p.Sq;
         m_run[t] = -CUDART_INF_F;
         l_run[t] = 0.f;
     }
-    // query rows (zero past R), and a zero P~ tile (rows past R stay zero)
-    const int ld = __ffs(D) - 1;  // D is a power of two
-    for (int e = t; e < 8 * NT * D; e += kThreads) {
-        const int r = e >> ld, d = e & (D - 1);
-        T v = from_f<T>(0.f);
-        if (r < R)
-            v = (static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + r / p.Sq) * p.sq1 +
-                 (long long)(r % p.Sq) * p.sq2)[d];
-        qsh[r * D + 8 * swz(r, d / 8, uk) + d % 8] = v;
-    }
-    for (int e = t; e < 16 * kPthPitch; e += kThreads) pth[e] = from_f<T>(0.f);
-
-    // the output product: warp w owns value columns [8 ntw w, 8 ntw (w + 1))
-    const int nvt = Dv / 8;                      // 8-column tiles
-    const int ntw = nvt >= 8 ? nvt / 8 : 1;      // tiles per warp: 1, 2 or 4
-    const bool pv_warp = warp < (nvt >= 8 ? 8 : nvt);
-    float oc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) oc[i][e] = 0.f;
-
-    const uint32_t ring_u = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
-    const uint32_t qsh_u = static_cast<uint32_t>(__cvta_generic_to_shared(qsh));
-
-    for (int pc = 0; pc < npieces; ++pc) {
-        const int s = pc % slots;
-        // this thread's copies of piece pc have landed (those of the next
-        // slots - 1 pieces may still be in flight); the barrier makes every
-        // thread's copies, and the set-up above, visible
-        cp_async_wait_pieces(slots);
-        __syncthreads();
-        const uint32_t kslot = ring_u + s * p.slot_bytes;
-        const uint32_t vslot = kslot + kStreamTK * uk * 16;
-        const int j0 = pc * kStreamTK, tk = min(kStreamTK, n - j0);
-
-        // S^T = K Q^T on all eight warps: warp w takes key tile w & 1 (16 keys)
-        // and k-group w >> 1 (a quarter of the k-steps, alternating between two
-        // accumulators), so no chain of dependent instructions is longer than
-        // two; the groups' partial sums meet in the statistics phase
-        {
-            const int mt = warp & 1, kg = warp >> 1;
-            const int nks = D / 16, per = (nks + 3) / 4;
-            const int ks0 = min(nks, kg * per), ks1 = min(nks, ks0 + per);
-            float c[2][NT][4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int i = 0; i < NT; ++i) c[h][i][0] = c[h][i][1] = c[h][i][2] = c[h][i][3] = 0.f;
-            const int mi = lane >> 3, r8 = lane & 7;
-            const int key = 16 * mt + (mi & 1) * 8 + r8;  // this lane's row address for the K matrices
-            for (int ks2 = ks0; ks2 < ks1; ks2 += 2) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int ks = ks2 + h;
-                    if (ks >= ks1) break;
-                    uint32_t qb[NT][2];
-#pragma unroll
-                    for (int i = 0; i < NT; ++i) {
-                        const int qr = 8 * i + r8;  // lanes 0-15 address units 2 ks, 2 ks + 1
-                        ldsm_x2(qsh_u + 16 * (qr * uk + swz(qr, 2 * ks + (mi & 1), uk)), qb[i][0], qb[i][1]);
-                    }
-                    uint32_t a[4];
-                    ldsm_x4(kslot + 16 * (key * uk + swz(key, 2 * ks + (mi >> 1), uk)), a[0], a[1], a[2], a[3]);
-#pragma unroll
-                    for (int i = 0; i < NT; ++i) mma16816<T>(c[h][i], a, qb[i][0], qb[i][1]);
-                }
-            }
-            // c[.][i] = partial S^T[key 16 mt + g (+8)][row 8 i + 2 cc (+1)]
-#pragma unroll
-            for (int i = 0; i < NT; ++i)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = 8 * i + 2 * cc + (e & 1), kk = 16 * mt + g + 8 * (e >> 1);
-                    if (row < R) part[(kg * RM + row) * kStreamTK + kk] = c[0][i][e] + c[1][i][e];
-                }
-        }
-        __syncthreads();
-
-        // masking and the online statistics: one warp per row, one lane per key
-        for (int r = warp; r < R; r += kThreads / 32) {
-            float sv = -CUDART_INF_F;
-            if (lane < tk) {
-                const int key = k0 + j0 + lane;
-                const float* pr = part + r * kStreamTK + lane;
-                sv = __fmul_rn((pr[0] + pr[RM * kStreamTK]) + (pr[2 * RM * kStreamTK] + pr[3 * RM * kStreamTK]), p.c2);
-                if (p.causal && key > row_i[r]) sv = -CUDART_INF_F;
-                if (p.mask_kind != kMaskNone) {
-                    const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + key;
-                    if (p.mask_kind == kMaskBool) {
-                        if (static_cast<const unsigned char*>(p.mask)[off] == 0) sv = -CUDART_INF_F;
-                    } else {
-                        const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
-                                                             : to_f(static_cast<const T*>(p.mask)[off]);
-                        sv = __fmaf_rn(m, kLog2e, sv);
-                    }
-                }
-                ss[r * p.chunk + j0 + lane] = sv;
-            }
-            float mp = sv;
-            for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-            const float mo = m_run[r];
-            const float mn = fmaxf(mo, mp);
-            const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // a row with no visible key yet adds zeros
-            const float e = ptx::ex2(sv - ms);  // sv = -inf gives 0
-            float sum = e;
-            for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-            pth[r * kPthPitch + lane] = from_f<T>(e);
-            if (lane == 0) {
-                const float al = ptx::ex2(mo - ms);
-                alpha_s[r] = al;
-                m_run[r] = mn;
-                l_run[r] = l_run[r] * al + sum;
-            }
-        }
-        __syncthreads();
-
-        // O += P~ V: rows g and g + 8 of each of this warp's column tiles
-        if (pv_warp) {
-            const float a_lo = g < R ? alpha_s[g] : 0.f, a_hi = g + 8 < R ? alpha_s[g + 8] : 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (i < ntw) {
-                    oc[i][0] *= a_lo; oc[i][1] *= a_lo;
-                    oc[i][2] *= a_hi; oc[i][3] *= a_hi;
-                }
-            const int mi = lane >> 3, r8 = lane & 7;
-#pragma unroll
-            for (int ks = 0; ks < kStreamTK / 16; ++ks) {
-                uint32_t a[4];
-                a[0] = *reinterpret_cast<const uint32_t*>(&pth[g * kPthPitch + 16 * ks + 2 * cc]);
-                a[1] = *reinterpret_cast<const uint32_t*>(&pth[(g + 8) * kPthPitch + 16 * ks + 2 * cc]);
-                a[2] = *reinterpret_cast<const uint32_t*>(&pth[g * kPthPitch + 16 * ks + 8 + 2 * cc]);
-                a[3] = *reinterpret_cast<const uint32_t*>(&pth[(g + 8) * kPthPitch + 16 * ks + 8 + 2 * cc]);
-                const int key = 16 * ks + (mi & 1) * 8 + r8;  // this lane's row address for the V matrices
-                if (ntw == 1) {
-                    uint32_t b0, b1;
-                    ldsm_x2_t(vslot + 16 * (key * uv + swz(key, warp, uv)), b0, b1);
-                    mma16816<T>(oc[0], a, b0, b1);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 4; i += 2)
-                        if (i < ntw) {
-                            uint32_t b0, b1, b2, b3;
-                            const int unit = warp * ntw + i + (mi >> 1);
-                            ldsm_x4_t(vslot + 16 * (key * uv + swz(key, unit, uv)), b0, b1, b2, b3);
-                            mma16816<T>(oc[i], a, b0, b1);
-                            mma16816<T>(oc[i + 1], a, b2, b3);
-                        }
-                }
-            }
-        }
-        __syncthreads();  // the slot and the piece's P~ are free again
-        if (pc + slots < npieces) stream_issue(p, K, V, pc + slots, n, ring + s * p.slot_bytes, t);
-        else cp_async_commit();
-    }
-    cp_async_wait_all();
+    for (int e = t; e < 2 * 16 * kPthPitch; e += kThreads) pth[e] = from_f<T>(0.f);  // rows past R stay zero
     __syncthreads();
 
-    // the chunk's partial O (every element owned by one lane of one warp)
-    if (pv_warp) {
+    // the output product: warp 4 + w owns value-column tiles [ntw w, ntw (w + 1))
+    const int nvt = Dv / 8;                  // 8-column tiles
+    const int ntw = nvt >= 4 ? nvt / 4 : 1;  // tiles per warp: 1, 2, 4 or 8
+    const bool pv_warp = !copy_group && warp - 4 < (nvt >= 4 ? 4 : nvt);
+
+    if (copy_group) {
+        // ---- warps 0-3: copies, S^T = K Q^T and the online statistics, one
+        // piece ahead of the output product.  Warp w takes key tile w & 1 and
+        // k-group w >> 1 (half the k-steps, two accumulators); its Q^T
+        // fragments stay in registers.
+        const int mt = warp & 1, kg = warp >> 1;
+        const int per = D / 32;  // k-steps per group: 1, 2, 4 or 8
+        uint32_t qb[NT][8][2];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (i < ntw) {
-                const int col = 8 * (warp * ntw + i) + 2 * cc;
-                if (g < R) *reinterpret_cast<float2*>(&op[g * Dv + col]) = make_float2(oc[i][0], oc[i][1]);
-                if (g + 8 < R) *reinterpret_cast<float2*>(&op[(g + 8) * Dv + col]) = make_float2(oc[i][2], oc[i][3]);
+        for (int i = 0; i < NT; ++i)
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                qb[i][s][0] = qb[i][s][1] = 0u;
+                const int qr = 8 * i + g;
+                if (s < per && qr < R) {
+                    const unsigned short* qrow = reinterpret_cast<const unsigned short*>(
+                        static_cast<const T*>(p.q) + b * p.sq0 + (long long)(hk * p.group + qr / p.Sq) * p.sq1 +
+                        (long long)(qr % p.Sq) * p.sq2);
+                    const int d = 16 * (kg * per + s) + 2 * cc;
+                    qb[i][s][0] = (uint32_t)qrow[d] | ((uint32_t)qrow[d + 1] << 16);
+                    qb[i][s][1] = (uint32_t)qrow[d + 8] | ((uint32_t)qrow[d + 9] << 16);
+                }
             }
+        const int key = 16 * mt + (mi & 1) * 8 + r8;  // this lane's row address for the K matrices
+        for (int i = 0; i < npieces; ++i) {
+            // this thread's copies of piece i have landed (those of piece i + 1
+            // may still be in flight); the group barrier shares everyone's
+            cp_async_wait_pieces(2);
+            nbar_sync<kBarGroup, kGroupThreads>();
+            const uint32_t kslot = static_cast<uint32_t>(__cvta_generic_to_shared(kring + (i & 1) * kbytes));
+            const int j0 = i * kStreamTK, tk = min(kStreamTK, n - j0);
+            {
+                float c[2][NT][4];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int q = 0; q < NT; ++q) c[h][q][0] = c[h][q][1] = c[h][q][2] = c[h][q][3] = 0.f;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    if (s >= per) break;
+                    uint32_t a[4];
+                    ldsm_x4(kslot + 16 * (key * uk + swz(key, 2 * (kg * per + s) + (mi >> 1), uk)), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                    for (int q = 0; q < NT; ++q) mma16816<T>(c[s & 1][q], a, qb[q][s][0], qb[q][s][1]);
+                }
+#pragma unroll
+                for (int q = 0; q < NT; ++q)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = 8 * q + 2 * cc + (e & 1), kk = 16 * mt + g + 8 * (e >> 1);
+                        if (row < R) part[(kg * RM + row) * kStreamTK + kk] = c[0][q][e] + c[1][q][e];
+                    }
+            }
+            nbar_sync<kBarGroup, kGroupThreads>();
+            // P~ tile and rescale factors of piece i - 2 are free once its P V is done
+            if (i >= 2) free_sync(i);
+            T* pt = pth + (i & 1) * 16 * kPthPitch;
+            for (int r = warp; r < R; r += 4) {
+                float sv = -CUDART_INF_F;
+                if (lane < tk) {
+                    const int kglob = k0 + j0 + lane;
+                    const float* pr = part + r * kStreamTK + lane;
+                    sv = __fmul_rn(pr[0] + pr[RM * kStreamTK], p.c2);
+                    if (p.causal && kglob > row_i[r]) sv = -CUDART_INF_F;
+                    if (p.mask_kind != kMaskNone) {
+                        const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + kglob;
+                        if (p.mask_kind == kMaskBool) {
+                            if (static_cast<const unsigned char*>(p.mask)[off] == 0) sv = -CUDART_INF_F;
+                        } else {
+                            const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                                 : to_f(static_cast<const T*>(p.mask)[off]);
+                            sv = __fmaf_rn(m, kLog2e, sv);
+                        }
+                    }
+                    ss[r * p.chunk + j0 + lane] = sv;
+                }
+                float mp = sv;
+                for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+                const float mo = m_run[r];
+                const float mn = fmaxf(mo, mp);
+                const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // a row with no visible key yet adds zeros
+                const float e = ptx::ex2(sv - ms);                 // sv = -inf gives 0
+                float sum = e;
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                pt[r * kPthPitch + lane] = from_f<T>(e);
+                if (lane == 0) {
+                    const float al = ptx::ex2(mo - ms);
+                    alpha_s[i & 1][r] = al;
+                    m_run[r] = mn;
+                    l_run[r] = l_run[r] * al + sum;
+                }
+            }
+            // piece i + 2: K into this piece's K slot (its scores are done), V
+            // into the slot piece i - 2 used (its P V is done)
+            if (i + 2 < npieces)
+                stream_issue(p, K, V, i + 2, n, kring + (i & 1) * kbytes, vring + ((i + 2) & 3) * vbytes, t);
+            else
+                cp_async_commit();
+            full_arrive(i);
+        }
+        // the output product's last releases
+        for (int i = max(0, npieces - 2); i < npieces; ++i) free_sync(i);
+        cp_async_wait_all();
+    } else {
+        // ---- warps 4-7: O += P~ V, rows g and g + 8 of each of this warp's
+        // column tiles, one piece behind the statistics
+        const int wb = warp - 4;
+        float oc[8][4];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oc[q][e] = 0.f;
+        for (int i = 0; i < npieces; ++i) {
+            full_sync(i);
+            if (pv_warp) {
+                const float a_lo = g < R ? alpha_s[i & 1][g] : 0.f, a_hi = g + 8 < R ? alpha_s[i & 1][g + 8] : 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    if (q < ntw) {
+                        oc[q][0] *= a_lo; oc[q][1] *= a_lo;
+                        oc[q][2] *= a_hi; oc[q][3] *= a_hi;
+                    }
+                const uint32_t vslot = static_cast<uint32_t>(__cvta_generic_to_shared(vring + (i & 3) * vbytes));
+                const T* pt = pth + (i & 1) * 16 * kPthPitch;
+#pragma unroll
+                for (int ks = 0; ks < kStreamTK / 16; ++ks) {
+                    uint32_t a[4];
+                    a[0] = *reinterpret_cast<const uint32_t*>(&pt[g * kPthPitch + 16 * ks + 2 * cc]);
+                    a[1] = *reinterpret_cast<const uint32_t*>(&pt[(g + 8) * kPthPitch + 16 * ks + 2 * cc]);
+                    a[2] = *reinterpret_cast<const uint32_t*>(&pt[g * kPthPitch + 16 * ks + 8 + 2 * cc]);
+                    a[3] = *reinterpret_cast<const uint32_t*>(&pt[(g + 8) * kPthPitch + 16 * ks + 8 + 2 * cc]);
+                    const int vkey = 16 * ks + (mi & 1) * 8 + r8;  // this lane's row address for the V matrices
+                    if (ntw == 1) {
+                        uint32_t b0, b1;
+                        ldsm_x2_t(vslot + 16 * (vkey * uv + swz(vkey, wb, uv)), b0, b1);
+                        mma16816<T>(oc[0], a, b0, b1);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 8; q += 2)
+                            if (q < ntw) {
+                                uint32_t b0, b1, b2, b3;
+                                const int unit = wb * ntw + q + (mi >> 1);
+                                ldsm_x4_t(vslot + 16 * (vkey * uv + swz(vkey, unit, uv)), b0, b1, b2, b3);
+                                mma16816<T>(oc[q], a, b0, b1);
+                                mma16816<T>(oc[q + 1], a, b2, b3);
+                            }
+                    }
+                }
+            }
+            free_arrive(i);
+        }
+        // the chunk's partial O, over the rings: the last piece's copies
+        // landed and its scores were done before its P~ was handed over
+        if (pv_warp) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q < ntw) {
+                    const int col = 8 * (wb * ntw + q) + 2 * cc;
+                    if (g < R) *reinterpret_cast<float2*>(&op[g * Dv + col]) = make_float2(oc[q][0], oc[q][1]);
+                    if (g + 8 < R)
+                        *reinterpret_cast<float2*>(&op[(g + 8) * Dv + col]) = make_float2(oc[q][2], oc[q][3]);
+                }
+        }
     }
+    __syncthreads();
     if (t < R) {
         st[2 * t] = m_run[t];
         st[2 * t + 1] = l_run[t];
@@ -1114,44 +1142,37 @@ cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Shared-memory layout of stream_decode_kernel (the ring gets as many slots,
-// up to four, as keep the CTA within four per SM); false when even two slots
-// exceed the budget.
+// Shared-memory layout of stream_decode_kernel: two K and four V slots of
+// 32-key pieces (the partial O reuses them after the loop), the chunk's
+// scores, two P~ tiles, the k-group partial scores and the merge area.  False
+// when it exceeds the budget.
 bool plan_stream(const Problem& p, DecParams* dp, int* smem) {
     int C, chunk, smem_cluster;
     DecParams tmp;
     plan(p, &C, &chunk, &tmp, &smem_cluster);
     const long long R = p.group * p.Sq, es = elem_bytes(p.dtype);
-    const long long NT = R > 8 ? 2 : 1;
     const long long RM = R <= 4 ? 4 : (R <= 8 ? 8 : 16);  // the kernel's row bound
-    const long long slot = (long long)kStreamTK * (p.D + p.Dv) * es;
+    const long long rings = (long long)kStreamTK * (kKSlots * p.D + kVSlots * p.Dv) * es;
     auto al = [](long long x) { return (x + 15) & ~15ll; };
-    for (int slots = kStreamMaxSlots; slots >= 2; --slots) {
-        long long off = 0;
-        const long long off_ring = off;  // ring; after the loop, the partial O
-        off = al(off + std::max((long long)slots * slot, R * p.Dv * 4));
-        const long long off_s = off; off = al(off + R * chunk * 4);
-        const long long off_q = off; off = al(off + 8 * NT * p.D * es);
-        const long long off_pt = off; off = al(off + 16 * kPthPitch * es);
-        const long long off_part = off; off = al(off + 4 * RM * kStreamTK * 4);
-        const long long off_st = off; off = al(off + R * 2 * 4);
-        const long long off_fac = off; off += R * C * 4;
-        if (off > kStreamSmemTarget && slots > 2) continue;
-        if (off > kSmemBudget) return false;
-        dp->slots = slots;
-        dp->slot_bytes = (int)slot;
-        dp->off_ring = (int)off_ring;
-        dp->off_s = (int)off_s;
-        dp->off_q = (int)off_q;
-        dp->off_pt = (int)off_pt;
-        dp->off_part = (int)off_part;
-        dp->off_stat = (int)off_st;
-        dp->off_fac = (int)off_fac;
-        dp->chunk = chunk;
-        *smem = (int)off;
-        return true;
-    }
-    return false;
+    long long off = 0;
+    const long long off_ring = off; off = al(off + std::max(rings, R * p.Dv * 4));
+    const long long off_s = off; off = al(off + R * chunk * 4);
+    const long long off_pt = off; off = al(off + 2 * 16 * kPthPitch * es);
+    const long long off_part = off; off = al(off + 2 * RM * kStreamTK * 4);
+    const long long off_st = off; off = al(off + R * 2 * 4);
+    const long long off_fac = off; off += R * C * 4;
+    if (off > kSmemBudget) return false;
+    dp->slots = kKSlots + kVSlots;
+    dp->slot_bytes = (int)rings;
+    dp->off_ring = (int)off_ring;
+    dp->off_s = (int)off_s;
+    dp->off_pt = (int)off_pt;
+    dp->off_part = (int)off_part;
+    dp->off_stat = (int)off_st;
+    dp->off_fac = (int)off_fac;
+    dp->chunk = chunk;
+    *smem = (int)off;
+    return true;
 }
 
 bool pow2_head_dim(int64_t d) { return d == 32 || d == 64 || d == 128 || d == 256; }

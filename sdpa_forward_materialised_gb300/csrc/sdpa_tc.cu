@@ -2790,9 +2790,12 @@ bool encode_map(CUtensorMap* map, int dtype, const void* base, long long X, long
     // becomes an extent-1 dimension whose coordinate is always 0 (code 0)
     for (auto& x : d)
         if (x.ext > 1 && x.stride == 0) { x.ext = 1; x.sel = 0; }
-    // extent-1 dims never move: give them a stride past everything else
+    // extent-1 dims never move: give them a stride past everything else,
+    // rounded up to the 16 bytes every tensor-map stride needs (a single P
+    // row of 698 keys, say, is still a valid map)
     long long maxb = X;
     for (auto& x : d) if (x.ext > 1) maxb = std::max(maxb, x.stride * x.ext);
+    maxb = (maxb + 7) / 8 * 8;
     for (auto& x : d) if (x.ext <= 1) x.stride = maxb;
     std::stable_sort(d, d + 3, [](const Dim& a, const Dim& c) { return a.stride < c.stride; });
     cuuint64_t dims[4] = {(cuuint64_t)X, 0, 0, 0};
