@@ -399,6 +399,7 @@ constexpr int kPthPitch = kStreamTK + 8;  // P~ tile row pitch (elements): confl
 constexpr int kKSlots = 2, kVSlots = 4;   // K / V ring slots (32-key pieces)
 constexpr int kGroupThreads = 128;        // each of the two warp groups
 constexpr int kBarGroup = 1, kBarFull = 2, kBarFree = 4;  // named barrier ids: copy group; [2] P~ ready; [2] P~ used
+constexpr int kBarPV = 6;                                  // P V group
 
 // Physical 16-byte unit of logical unit u in row `row` of a tile whose rows
 // hold `units` units (4, 8, 16 or 32): eight consecutive rows read at the same
@@ -436,39 +437,39 @@ __device__ __forceinline__ void mma16816<__nv_bfloat16>(float* c, const uint32_t
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Every thread of the copy group (warps 0-3): start its share of the copies
-// of piece `piece` of the chunk (K rows into K slot `kslot`, V rows into V
-// slot `vslot`, both swizzled) as 16-byte asynchronous copies and commit them
-// as one group.  V rows past the chunk's end get zeros (copies with no source
-// bytes), so P~ V never multiplies a zero by stale shared memory.
+// Every thread of one warp group: start its share of the 16-byte copies of
+// the K rows (issue_k) or the V rows (issue_v) of piece `piece` of the chunk
+// into a ring slot, each 16-byte unit u of row r at unit u ^ f(r), and commit
+// them as one group.  V rows past the chunk's end get zeros (copies with no
+// source bytes), so P~ V never multiplies a zero by stale shared memory.
 template <typename T>
-__device__ __forceinline__ void stream_issue(const DecParams& p, const T* K, const T* V, int piece, int n,
-                                             uint8_t* kslot, uint8_t* vslot, int ta) {
-    const int j0 = piece * kStreamTK;
-    const int tk = min(kStreamTK, n - j0);
-    const int uk = p.D * (int)sizeof(T) / 16, uv = p.Dv * (int)sizeof(T) / 16;  // 16-byte units per row
-    const int lk = __ffs(uk) - 1, lv = __ffs(uv) - 1;
+__device__ __forceinline__ void issue_rows(const T* X, long long sx, bool contig, int units, int j0, int tk,
+                                           int rows, uint8_t* slot, int ta) {
+    const int lu = __ffs(units) - 1;
     // rows back to back (row stride == head dim): the piece is one contiguous
     // block and unit c of it sits at byte 16 c
-    const uint8_t* kp = reinterpret_cast<const uint8_t*>(K + (long long)j0 * p.sk2);
-    const uint8_t* vp = reinterpret_cast<const uint8_t*>(V + (long long)j0 * p.sv2);
-    for (int c = ta; c < tk * uk; c += kGroupThreads) {
-        const int r = c >> lk, u = c & (uk - 1);
-        cp_async16(kslot + 16 * (r * uk + swz(r, u, uk)),
-                   p.k_contig ? kp + 16 * c : reinterpret_cast<const uint8_t*>(K + (long long)(j0 + r) * p.sk2) + 16 * u);
-    }
-    for (int c = ta; c < kStreamTK * uv; c += kGroupThreads) {
-        const int r = c >> lv, u = c & (uv - 1);
-        uint8_t* dst = vslot + 16 * (r * uv + swz(r, u, uv));
+    const uint8_t* xp = reinterpret_cast<const uint8_t*>(X + (long long)j0 * sx);
+    for (int c = ta; c < rows * units; c += kGroupThreads) {
+        const int r = c >> lu, u = c & (units - 1);
+        uint8_t* dst = slot + 16 * (r * units + swz(r, u, units));
         if (r < tk) {
-            cp_async16(dst, p.v_contig ? vp + 16 * c
-                                       : reinterpret_cast<const uint8_t*>(V + (long long)(j0 + r) * p.sv2) + 16 * u);
+            cp_async16(dst, contig ? xp + 16 * c : reinterpret_cast<const uint8_t*>(X + (long long)(j0 + r) * sx) + 16 * u);
         } else {
             const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(d), "l"(V) : "memory");
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, 0;" ::"r"(d), "l"(X) : "memory");
         }
     }
     cp_async_commit();
+}
+template <typename T>
+__device__ __forceinline__ void issue_k(const DecParams& p, const T* K, int piece, int n, uint8_t* slot, int ta) {
+    const int j0 = piece * kStreamTK, tk = min(kStreamTK, n - j0);
+    issue_rows(K, p.sk2, p.k_contig != 0, p.D * (int)sizeof(T) / 16, j0, tk, tk, slot, ta);
+}
+template <typename T>
+__device__ __forceinline__ void issue_v(const DecParams& p, const T* V, int piece, int n, uint8_t* slot, int ta) {
+    const int j0 = piece * kStreamTK, tk = min(kStreamTK, n - j0);
+    issue_rows(V, p.sv2, p.v_contig != 0, p.Dv * (int)sizeof(T) / 16, j0, tk, kStreamTK, slot, ta);
 }
 
 // Named barriers (immediate ids, so the kernel reserves only those it uses):
@@ -532,11 +533,18 @@ stream_decode_kernel(const DecParams p) {
     const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
     const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
 
-    if (copy_group)
-        for (int pc = 0; pc < 2; ++pc) {
-            if (pc < npieces) stream_issue(p, K, V, pc, n, kring + (pc & 1) * kbytes, vring + (pc & 3) * vbytes, t);
+    // K of pieces 0, 1 (warps 0-3) and V of pieces 0-3 (warps 4-7)
+    if (copy_group) {
+        for (int pc = 0; pc < kKSlots; ++pc) {
+            if (pc < npieces) issue_k(p, K, pc, n, kring + pc * kbytes, t);
             else cp_async_commit();
         }
+    } else {
+        for (int pc = 0; pc < kVSlots; ++pc) {
+            if (pc < npieces) issue_v(p, V, pc, n, vring + pc * vbytes, t - kGroupThreads);
+            else cp_async_commit();
+        }
+    }
     if (t < R) {
         row_h[t] = hk * p.group + t / p.Sq;
         row_i[t] = t % p.Sq;
@@ -552,7 +560,7 @@ stream_decode_kernel(const DecParams p) {
     const bool pv_warp = !copy_group && warp - 4 < (nvt >= 4 ? 4 : nvt);
 
     if (copy_group) {
-        // ---- warps 0-3: copies, S^T = K Q^T and the online statistics, one
+        // ---- warps 0-3: K copies, S^T = K Q^T and the online statistics, one
         // piece ahead of the output product.  Warp w takes key tile w & 1 and
         // k-group w >> 1 (half the k-steps, two accumulators); its Q^T
         // fragments stay in registers.
@@ -576,8 +584,8 @@ stream_decode_kernel(const DecParams p) {
             }
         const int key = 16 * mt + (mi & 1) * 8 + r8;  // this lane's row address for the K matrices
         for (int i = 0; i < npieces; ++i) {
-            // this thread's copies of piece i have landed (those of piece i + 1
-            // may still be in flight); the group barrier shares everyone's
+            // this thread's K copies of piece i have landed (those of piece
+            // i + 1 may still be in flight); the group barrier shares everyone's
             cp_async_wait_pieces(2);
             nbar_sync<kBarGroup, kGroupThreads>();
             const uint32_t kslot = static_cast<uint32_t>(__cvta_generic_to_shared(kring + (i & 1) * kbytes));
@@ -643,12 +651,9 @@ stream_decode_kernel(const DecParams p) {
                     l_run[r] = l_run[r] * al + sum;
                 }
             }
-            // piece i + 2: K into this piece's K slot (its scores are done), V
-            // into the slot piece i - 2 used (its P V is done)
-            if (i + 2 < npieces)
-                stream_issue(p, K, V, i + 2, n, kring + (i & 1) * kbytes, vring + ((i + 2) & 3) * vbytes, t);
-            else
-                cp_async_commit();
+            // K of piece i + 2 into this piece's K slot (its scores are done)
+            if (i + 2 < npieces) issue_k(p, K, i + 2, n, kring + (i & 1) * kbytes, t);
+            else cp_async_commit();
             full_arrive(i);
         }
         // the output product's last releases
@@ -664,6 +669,11 @@ stream_decode_kernel(const DecParams p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) oc[q][e] = 0.f;
         for (int i = 0; i < npieces; ++i) {
+            // this thread's V copies of piece i have landed (those of the next
+            // three pieces may still be in flight); the group barrier shares
+            // everyone's
+            cp_async_wait_pieces(4);
+            nbar_sync<kBarPV, kGroupThreads>();
             full_sync(i);
             if (pv_warp) {
                 const float a_lo = g < R ? alpha_s[i & 1][g] : 0.f, a_hi = g + 8 < R ? alpha_s[i & 1][g + 8] : 0.f;
@@ -701,9 +711,14 @@ stream_decode_kernel(const DecParams p) {
                 }
             }
             free_arrive(i);
+            // V of piece i + 4 into this piece's V slot, once every warp of the
+            // group is done with it
+            nbar_sync<kBarPV, kGroupThreads>();
+            if (i + kVSlots < npieces) issue_v(p, V, i + kVSlots, n, vring + (i & 3) * vbytes, t - kGroupThreads);
+            else cp_async_commit();
         }
-        // the chunk's partial O, over the rings: the last piece's copies
-        // landed and its scores were done before its P~ was handed over
+        // the chunk's partial O, over the rings: every K copy landed before
+        // the last scores, every V copy before the last P V
         if (pv_warp) {
 #pragma unroll
             for (int q = 0; q < 8; ++q)
