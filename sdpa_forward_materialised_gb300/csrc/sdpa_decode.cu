@@ -373,22 +373,25 @@ decode_kernel(const DecParams p) {
 //
 // The cluster split of decode_kernel (one cluster per (batch, key/value head),
 // CTA rank c owns a contiguous chunk of keys), with another data path inside
-// the CTA:
-//   * K and V stream through a ring of 32-key pieces.  Every thread issues
-//     16-byte asynchronous copies (consecutive threads on consecutive bytes of
-//     a row) and places each 16-byte unit of a row at unit u ^ f(row), an XOR
-//     swizzle that makes the 8-row matrix loads below conflict-free.  A slot
-//     is refilled as soon as the CTA has used it, so each CTA keeps a few
-//     pieces in flight from its first instructions on;
+// the CTA, in two warp groups one 32-key piece apart:
+//   * warps 0-3 stream K through a two-slot ring (two pieces ahead) and form
+//     the scores S^T = K_piece Q^T and the chunk's online softmax of piece i:
+//     one warp per row and one lane per key keep the running (max, sum), and
+//     P~ = exp2(s - running max), rounded to the input dtype, goes into one of
+//     two P~ tiles with its rescale factors.  The scores stay in shared memory
+//     for P;
+//   * warps 4-7 stream V through a four-slot ring (four pieces ahead) and
+//     accumulate O += P~ V of piece i - 1, rescaling O whenever the max grew;
+//   * the groups pass the P~ tiles back and forth through double-buffered
+//     named barriers (bar.arrive by the producing group, bar.sync by the
+//     consuming one); each group waits only for its own asynchronous copies;
+//   * copies are 16-byte cp.async (consecutive threads on consecutive bytes of
+//     a row), each 16-byte unit of a row placed at unit u ^ f(row), an XOR
+//     swizzle that makes the 8-row matrix loads conflict-free;
 //   * both products run on the tensor cores with the warp-level
-//     mma.sync.m16n8k16 (fp16 / bf16 operands, fp32 accumulation): the scores
-//     as S^T = K_piece Q^T (16 keys by 8 query rows per instruction), the
-//     output as O += P~ V (the query rows padded to 16, 8 value columns per
-//     instruction);
-//   * the chunk's softmax runs online: one warp per row and one lane per key
-//     keep the running (max, sum); P~ = exp2(s - running max), rounded to the
-//     input dtype, is the A operand of P V, and O is rescaled whenever the
-//     max grows.  The scores stay in shared memory for P;
+//     mma.sync.m16n8k16 (fp16 / bf16 operands, fp32 accumulation): 16 keys by
+//     8 query rows per score instruction, the query rows padded to 16 and 8
+//     value columns per output instruction;
 //   * one cluster barrier publishes every CTA's (max, sum) and partial O.
 //     Each CTA then forms the same lse, writes its P = exp2(s - lse) and sums
 //     its slice of the O columns over the cluster, the partial of CTA c
