@@ -380,7 +380,7 @@ decode_kernel(const DecParams p) {
 //     P~ = exp2(s - running max), rounded to the input dtype, goes into one of
 //     two P~ tiles with its rescale factors.  The scores stay in shared memory
 //     for P;
-//   * warps 4-7 stream V through a four-slot ring (four pieces ahead) and
+//   * warps 4-7 stream V through a three-slot ring (two pieces ahead) and
 //     accumulate O += P~ V of piece i - 1, rescaling O whenever the max grew;
 //   * the groups pass the P~ tiles back and forth through double-buffered
 //     named barriers (bar.arrive by the producing group, bar.sync by the
@@ -399,7 +399,7 @@ decode_kernel(const DecParams p) {
 // ---------------------------------------------------------------------------
 constexpr int kStreamTK = 32;   // keys per piece (one per lane in the row statistics)
 constexpr int kPthPitch = kStreamTK + 8;  // P~ tile row pitch (elements): conflict-free fragment loads
-constexpr int kKSlots = 2, kVSlots = 4;   // K / V ring slots (32-key pieces)
+constexpr int kKSlots = 2, kVSlots = 3;   // K / V ring slots (32-key pieces)
 constexpr int kGroupThreads = 128;        // each of the two warp groups
 constexpr int kBarGroup = 1, kBarFull = 2, kBarFree = 4;  // named barrier ids: copy group; [2] P~ ready; [2] P~ used
 constexpr int kBarPV = 6;                                  // P V group
@@ -536,17 +536,11 @@ stream_decode_kernel(const DecParams p) {
     const T* K = static_cast<const T*>(p.k) + b * p.sk0 + hk * p.sk1 + (long long)k0 * p.sk2;
     const T* V = static_cast<const T*>(p.v) + b * p.sv0 + hk * p.sv1 + (long long)k0 * p.sv2;
 
-    // K of pieces 0, 1 (warps 0-3) and V of pieces 0-3 (warps 4-7)
-    if (copy_group) {
-        for (int pc = 0; pc < kKSlots; ++pc) {
-            if (pc < npieces) issue_k(p, K, pc, n, kring + pc * kbytes, t);
-            else cp_async_commit();
-        }
-    } else {
-        for (int pc = 0; pc < kVSlots; ++pc) {
-            if (pc < npieces) issue_v(p, V, pc, n, vring + pc * vbytes, t - kGroupThreads);
-            else cp_async_commit();
-        }
+    // K (warps 0-3) and V (warps 4-7) of pieces 0 and 1
+    for (int pc = 0; pc < 2; ++pc) {
+        if (pc >= npieces) cp_async_commit();
+        else if (copy_group) issue_k(p, K, pc, n, kring + pc * kbytes, t);
+        else issue_v(p, V, pc, n, vring + pc * vbytes, t - kGroupThreads);
     }
     if (t < R) {
         row_h[t] = hk * p.group + t / p.Sq;
@@ -672,11 +666,14 @@ stream_decode_kernel(const DecParams p) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) oc[q][e] = 0.f;
         for (int i = 0; i < npieces; ++i) {
-            // this thread's V copies of piece i have landed (those of the next
-            // three pieces may still be in flight); the group barrier shares
-            // everyone's
-            cp_async_wait_pieces(4);
+            // this thread's V copies of piece i have landed (those of piece
+            // i + 1 may still be in flight); the group barrier shares everyone's
+            // and ends every warp's P V of piece i - 1, so V of piece i + 2
+            // can take that piece's slot
+            cp_async_wait_pieces(2);
             nbar_sync<kBarPV, kGroupThreads>();
+            if (i + 2 < npieces) issue_v(p, V, i + 2, n, vring + ((i + 2) % kVSlots) * vbytes, t - kGroupThreads);
+            else cp_async_commit();
             full_sync(i);
             if (pv_warp) {
                 const float a_lo = g < R ? alpha_s[i & 1][g] : 0.f, a_hi = g + 8 < R ? alpha_s[i & 1][g + 8] : 0.f;
@@ -686,7 +683,7 @@ stream_decode_kernel(const DecParams p) {
                         oc[q][0] *= a_lo; oc[q][1] *= a_lo;
                         oc[q][2] *= a_hi; oc[q][3] *= a_hi;
                     }
-                const uint32_t vslot = static_cast<uint32_t>(__cvta_generic_to_shared(vring + (i & 3) * vbytes));
+                const uint32_t vslot = static_cast<uint32_t>(__cvta_generic_to_shared(vring + (i % kVSlots) * vbytes));
                 const T* pt = pth + (i & 1) * 16 * kPthPitch;
 #pragma unroll
                 for (int ks = 0; ks < kStreamTK / 16; ++ks) {
@@ -714,11 +711,6 @@ stream_decode_kernel(const DecParams p) {
                 }
             }
             free_arrive(i);
-            // V of piece i + 4 into this piece's V slot, once every warp of the
-            // group is done with it
-            nbar_sync<kBarPV, kGroupThreads>();
-            if (i + kVSlots < npieces) issue_v(p, V, i + kVSlots, n, vring + (i & 3) * vbytes, t - kGroupThreads);
-            else cp_async_commit();
         }
         // the chunk's partial O, over the rings: every K copy landed before
         // the last scores, every V copy before the last P V
@@ -1160,7 +1152,7 @@ cudaError_t launch_rm(const Problem& pr, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// Shared-memory layout of stream_decode_kernel: two K and four V slots of
+// Shared-memory layout of stream_decode_kernel: two K and three V slots of
 // 32-key pieces (the partial O reuses them after the loop), the chunk's
 // scores, two P~ tiles, the k-group partial scores and the merge area.  False
 // when it exceeds the budget.
