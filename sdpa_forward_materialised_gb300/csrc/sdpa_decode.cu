@@ -116,7 +116,7 @@ struct DecParams {
     float c2;  // scale * log2(e)
     int off_v, off_q, off_s, off_o, off_stat;  // shared-memory layout (bytes)
     // streaming kernel only
-    int slots, slot_bytes, off_ring, off_pt, off_fac, off_part;
+    int off_ring, off_pt, off_fac, off_part;
     int k_contig, v_contig;  // key / value rows back to back (row stride == head dim)
 };
 
@@ -1172,8 +1172,6 @@ bool plan_stream(const Problem& p, DecParams* dp, int* smem) {
     const long long off_st = off; off = al(off + R * 2 * 4);
     const long long off_fac = off; off += R * C * 4;
     if (off > kSmemBudget) return false;
-    dp->slots = kKSlots + kVSlots;
-    dp->slot_bytes = (int)rings;
     dp->off_ring = (int)off_ring;
     dp->off_s = (int)off_s;
     dp->off_pt = (int)off_pt;
