@@ -121,12 +121,8 @@ struct DecParams {
 };
 
 __device__ __forceinline__ void cp_async_wait_ring() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-// All but the newest slots - 1 committed groups of this thread are complete.
-__device__ __forceinline__ void cp_async_wait_pieces(int slots) {
-    if (slots >= 4) asm volatile("cp.async.wait_group 3;" ::: "memory");
-    else if (slots == 3) asm volatile("cp.async.wait_group 2;" ::: "memory");
-    else asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
+// Every committed group of this thread but the newest one is complete.
+__device__ __forceinline__ void cp_async_wait_all_but_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // RM is a compile-time bound on the query rows (R <= RM), so the per-row
 // accumulators of the score phase stay in registers.
@@ -583,7 +579,7 @@ stream_decode_kernel(const DecParams p) {
         for (int i = 0; i < npieces; ++i) {
             // this thread's K copies of piece i have landed (those of piece
             // i + 1 may still be in flight); the group barrier shares everyone's
-            cp_async_wait_pieces(2);
+            cp_async_wait_all_but_one();
             nbar_sync<kBarGroup, kGroupThreads>();
             const uint32_t kslot = static_cast<uint32_t>(__cvta_generic_to_shared(kring + (i & 1) * kbytes));
             const int j0 = i * kStreamTK, tk = min(kStreamTK, n - j0);
@@ -670,7 +666,7 @@ stream_decode_kernel(const DecParams p) {
             // i + 1 may still be in flight); the group barrier shares everyone's
             // and ends every warp's P V of piece i - 1, so V of piece i + 2
             // can take that piece's slot
-            cp_async_wait_pieces(2);
+            cp_async_wait_all_but_one();
             nbar_sync<kBarPV, kGroupThreads>();
             if (i + 2 < npieces) issue_v(p, V, i + 2, n, vring + ((i + 2) % kVSlots) * vbytes, t - kGroupThreads);
             else cp_async_commit();
