@@ -371,16 +371,18 @@ decode_kernel(const DecParams p) {
 // CTA rank c owns a contiguous chunk of keys), with another data path inside
 // the CTA, in two warp groups one 32-key piece apart:
 //   * warps 0-3 stream K through a two-slot ring (two pieces ahead) and form
-//     the scores S^T = K_piece Q^T and the chunk's online softmax of piece i:
-//     one warp per row and one lane per key keep the running (max, sum), and
-//     P~ = exp2(s - running max), rounded to the input dtype, goes into one of
-//     two P~ tiles with its rescale factors.  The scores stay in shared memory
-//     for P;
-//   * warps 4-7 stream V through a three-slot ring (two pieces ahead) and
-//     accumulate O += P~ V of piece i - 1, rescaling O whenever the max grew;
-//   * the groups pass the P~ tiles back and forth through double-buffered
-//     named barriers (bar.arrive by the producing group, bar.sync by the
-//     consuming one); each group waits only for its own asynchronous copies;
+//     the partial scores S^T = K_piece Q^T of piece i (two k-groups) in one of
+//     two shared buffers;
+//   * warps 4-7 stream V through a three-slot ring (two pieces ahead) and,
+//     for piece i - 1, run the masking and the chunk's online softmax (one
+//     warp per row and one lane per key keep the running (max, sum); P~ =
+//     exp2(s - running max), rounded to the input dtype, and the rescale
+//     factors go to shared memory; the scores stay there for P) and
+//     accumulate O += P~ V, rescaling O whenever the max grew;
+//   * the groups pass the score buffers back and forth through double-
+//     buffered named barriers (bar.arrive by the producing group, bar.sync by
+//     the consuming one); each group waits only for its own asynchronous
+//     copies;
 //   * copies are 16-byte cp.async (consecutive threads on consecutive bytes of
 //     a row), each 16-byte unit of a row placed at unit u ^ f(row), an XOR
 //     swizzle that makes the 8-row matrix loads conflict-free;
@@ -503,7 +505,7 @@ stream_decode_kernel(const DecParams p) {
     static_assert(sizeof(T) == 2, "16-bit inputs");
     constexpr int NT = RM > 8 ? 2 : 1;  // 8-row tiles of query rows in the score product
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float m_run[kMaxRows], l_run[kMaxRows], alpha_s[2][kMaxRows], lse_s[kMaxRows];
+    __shared__ float m_run[kMaxRows], l_run[kMaxRows], alpha_s[kMaxRows], lse_s[kMaxRows];
     __shared__ int row_h[kMaxRows], row_i[kMaxRows];
 
     const int t = threadIdx.x, warp = t / 32, lane = t % 32;
@@ -523,8 +525,8 @@ stream_decode_kernel(const DecParams p) {
     uint8_t* kring = smem + p.off_ring;               // [kKSlots][32 rows of K]
     uint8_t* vring = kring + kKSlots * kbytes;        // [kVSlots][32 rows of V]
     float* ss = reinterpret_cast<float*>(smem + p.off_s);      // [R][chunk] scores (base 2, masked)
-    T* pth = reinterpret_cast<T*>(smem + p.off_pt);            // [2][16][kPthPitch] P~ of a piece
-    float* part = reinterpret_cast<float*>(smem + p.off_part); // [2][RM][32] k-group partial scores
+    T* pth = reinterpret_cast<T*>(smem + p.off_pt);            // [16][kPthPitch] P~ of a piece
+    float* part = reinterpret_cast<float*>(smem + p.off_part); // [2][2][RM][32] k-group partial scores of a piece
     float* op = reinterpret_cast<float*>(smem + p.off_ring);   // [R][Dv] partial O (the rings, after the loop)
     float* st = reinterpret_cast<float*>(smem + p.off_stat);   // [R][2] chunk (max, sum)
     float* fac = reinterpret_cast<float*>(smem + p.off_fac);   // [R][C] weight of each CTA's partial O
@@ -544,7 +546,7 @@ stream_decode_kernel(const DecParams p) {
         m_run[t] = -CUDART_INF_F;
         l_run[t] = 0.f;
     }
-    for (int e = t; e < 2 * 16 * kPthPitch; e += kThreads) pth[e] = from_f<T>(0.f);  // rows past R stay zero
+    for (int e = t; e < 16 * kPthPitch; e += kThreads) pth[e] = from_f<T>(0.f);  // rows past R stay zero
     __syncthreads();
 
     // the output product: warp 4 + w owns value-column tiles [ntw w, ntw (w + 1))
@@ -553,8 +555,8 @@ stream_decode_kernel(const DecParams p) {
     const bool pv_warp = !copy_group && warp - 4 < (nvt >= 4 ? 4 : nvt);
 
     if (copy_group) {
-        // ---- warps 0-3: K copies, S^T = K Q^T and the online statistics, one
-        // piece ahead of the output product.  Warp w takes key tile w & 1 and
+        // ---- warps 0-3: K copies and S^T = K Q^T, one piece ahead of the
+        // statistics and the output product.  Warp w takes key tile w & 1 and
         // k-group w >> 1 (half the k-steps, two accumulators); its Q^T
         // fragments stay in registers.
         const int mt = warp & 1, kg = warp >> 1;
@@ -581,8 +583,10 @@ stream_decode_kernel(const DecParams p) {
             // i + 1 may still be in flight); the group barrier shares everyone's
             cp_async_wait_all_but_one();
             nbar_sync<kBarGroup, kGroupThreads>();
+            // the partial-score buffer of piece i - 2 is free once its statistics are done
+            if (i >= 2) free_sync(i);
             const uint32_t kslot = static_cast<uint32_t>(__cvta_generic_to_shared(kring + (i & 1) * kbytes));
-            const int j0 = i * kStreamTK, tk = min(kStreamTK, n - j0);
+            float* pp = part + (i & 1) * 2 * RM * kStreamTK;
             {
                 float c[2][NT][4];
 #pragma unroll
@@ -602,59 +606,22 @@ stream_decode_kernel(const DecParams p) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int row = 8 * q + 2 * cc + (e & 1), kk = 16 * mt + g + 8 * (e >> 1);
-                        if (row < R) part[(kg * RM + row) * kStreamTK + kk] = c[0][q][e] + c[1][q][e];
+                        if (row < R) pp[(kg * RM + row) * kStreamTK + kk] = c[0][q][e] + c[1][q][e];
                     }
             }
-            nbar_sync<kBarGroup, kGroupThreads>();
-            // P~ tile and rescale factors of piece i - 2 are free once its P V is done
-            if (i >= 2) free_sync(i);
-            T* pt = pth + (i & 1) * 16 * kPthPitch;
-            for (int r = warp; r < R; r += 4) {
-                float sv = -CUDART_INF_F;
-                if (lane < tk) {
-                    const int kglob = k0 + j0 + lane;
-                    const float* pr = part + r * kStreamTK + lane;
-                    sv = __fmul_rn(pr[0] + pr[RM * kStreamTK], p.c2);
-                    if (p.causal && kglob > row_i[r]) sv = -CUDART_INF_F;
-                    if (p.mask_kind != kMaskNone) {
-                        const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + kglob;
-                        if (p.mask_kind == kMaskBool) {
-                            if (static_cast<const unsigned char*>(p.mask)[off] == 0) sv = -CUDART_INF_F;
-                        } else {
-                            const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
-                                                                 : to_f(static_cast<const T*>(p.mask)[off]);
-                            sv = __fmaf_rn(m, kLog2e, sv);
-                        }
-                    }
-                    ss[r * p.chunk + j0 + lane] = sv;
-                }
-                float mp = sv;
-                for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
-                const float mo = m_run[r];
-                const float mn = fmaxf(mo, mp);
-                const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // a row with no visible key yet adds zeros
-                const float e = ptx::ex2(sv - ms);                 // sv = -inf gives 0
-                float sum = e;
-                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                pt[r * kPthPitch + lane] = from_f<T>(e);
-                if (lane == 0) {
-                    const float al = ptx::ex2(mo - ms);
-                    alpha_s[i & 1][r] = al;
-                    m_run[r] = mn;
-                    l_run[r] = l_run[r] * al + sum;
-                }
-            }
+            nbar_sync<kBarGroup, kGroupThreads>();  // every warp is done with this K slot
             // K of piece i + 2 into this piece's K slot (its scores are done)
             if (i + 2 < npieces) issue_k(p, K, i + 2, n, kring + (i & 1) * kbytes, t);
             else cp_async_commit();
             full_arrive(i);
         }
-        // the output product's last releases
+        // the statistics' last releases
         for (int i = max(0, npieces - 2); i < npieces; ++i) free_sync(i);
         cp_async_wait_all();
     } else {
-        // ---- warps 4-7: O += P~ V, rows g and g + 8 of each of this warp's
-        // column tiles, one piece behind the statistics
+        // ---- warps 4-7: V copies, the masking and online statistics (one
+        // warp per row, one lane per key) and O += P~ V (rows g and g + 8 of
+        // each of this warp's column tiles), one piece behind the scores
         const int wb = warp - 4;
         float oc[8][4];
 #pragma unroll
@@ -671,8 +638,49 @@ stream_decode_kernel(const DecParams p) {
             if (i + 2 < npieces) issue_v(p, V, i + 2, n, vring + ((i + 2) % kVSlots) * vbytes, t - kGroupThreads);
             else cp_async_commit();
             full_sync(i);
+            {
+                const int j0 = i * kStreamTK, tk = min(kStreamTK, n - j0);
+                const float* pp = part + (i & 1) * 2 * RM * kStreamTK;
+                for (int r = wb; r < R; r += 4) {
+                    float sv = -CUDART_INF_F;
+                    if (lane < tk) {
+                        const int kglob = k0 + j0 + lane;
+                        const float* pr = pp + r * kStreamTK + lane;
+                        sv = __fmul_rn(pr[0] + pr[RM * kStreamTK], p.c2);
+                        if (p.causal && kglob > row_i[r]) sv = -CUDART_INF_F;
+                        if (p.mask_kind != kMaskNone) {
+                            const long long off = b * p.sm0 + row_h[r] * p.sm1 + (long long)row_i[r] * p.sm2 + kglob;
+                            if (p.mask_kind == kMaskBool) {
+                                if (static_cast<const unsigned char*>(p.mask)[off] == 0) sv = -CUDART_INF_F;
+                            } else {
+                                const float m = p.mask_dtype == kF32 ? static_cast<const float*>(p.mask)[off]
+                                                                     : to_f(static_cast<const T*>(p.mask)[off]);
+                                sv = __fmaf_rn(m, kLog2e, sv);
+                            }
+                        }
+                        ss[r * p.chunk + j0 + lane] = sv;
+                    }
+                    float mp = sv;
+                    for (int o = 16; o > 0; o >>= 1) mp = fmaxf(mp, __shfl_xor_sync(0xffffffffu, mp, o));
+                    const float mo = m_run[r];
+                    const float mn = fmaxf(mo, mp);
+                    const float ms = mn == -CUDART_INF_F ? 0.f : mn;  // a row with no visible key yet adds zeros
+                    const float e = ptx::ex2(sv - ms);                 // sv = -inf gives 0
+                    float sum = e;
+                    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                    pth[r * kPthPitch + lane] = from_f<T>(e);
+                    if (lane == 0) {
+                        const float al = ptx::ex2(mo - ms);
+                        alpha_s[r] = al;
+                        m_run[r] = mn;
+                        l_run[r] = l_run[r] * al + sum;
+                    }
+                }
+            }
+            free_arrive(i);                     // the partial scores of piece i are read
+            nbar_sync<kBarPV, kGroupThreads>();  // P~ and the rescale factors are complete
             if (pv_warp) {
-                const float a_lo = g < R ? alpha_s[i & 1][g] : 0.f, a_hi = g + 8 < R ? alpha_s[i & 1][g + 8] : 0.f;
+                const float a_lo = g < R ? alpha_s[g] : 0.f, a_hi = g + 8 < R ? alpha_s[g + 8] : 0.f;
 #pragma unroll
                 for (int q = 0; q < 8; ++q)
                     if (q < ntw) {
@@ -680,7 +688,7 @@ stream_decode_kernel(const DecParams p) {
                         oc[q][2] *= a_hi; oc[q][3] *= a_hi;
                     }
                 const uint32_t vslot = static_cast<uint32_t>(__cvta_generic_to_shared(vring + (i % kVSlots) * vbytes));
-                const T* pt = pth + (i & 1) * 16 * kPthPitch;
+                const T* pt = pth;
 #pragma unroll
                 for (int ks = 0; ks < kStreamTK / 16; ++ks) {
                     uint32_t a[4];
@@ -706,7 +714,6 @@ stream_decode_kernel(const DecParams p) {
                     }
                 }
             }
-            free_arrive(i);
         }
         // the chunk's partial O, over the rings: every K copy landed before
         // the last scores, every V copy before the last P V
@@ -1163,8 +1170,8 @@ bool plan_stream(const Problem& p, DecParams* dp, int* smem) {
     long long off = 0;
     const long long off_ring = off; off = al(off + std::max(rings, R * p.Dv * 4));
     const long long off_s = off; off = al(off + R * chunk * 4);
-    const long long off_pt = off; off = al(off + 2 * 16 * kPthPitch * es);
-    const long long off_part = off; off = al(off + 2 * RM * kStreamTK * 4);
+    const long long off_pt = off; off = al(off + 16 * kPthPitch * es);
+    const long long off_part = off; off = al(off + 2 * 2 * RM * kStreamTK * 4);
     const long long off_st = off; off = al(off + R * 2 * 4);
     const long long off_fac = off; off += R * C * 4;
     if (off > kSmemBudget) return false;
